@@ -1,0 +1,384 @@
+#!/usr/bin/env python
+"""Throughput of the INT8 quantized linear layer on GB300.
+
+One step = one full pass of the layer's hot path, ck_int8_linear: activation quantize
+(tensorwise: two passes), int8 -> bf16 weight widening, and the tensor-core GEMM with
+the fused dequant/bias/bf16 epilogue, over one batch of seeded synthetic inputs that
+are already resident in device memory.  Metric: 2*M*N*K / step time, in TOPS.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its own GPU
+(independent problems, weak scaling, no collective on the data path); the step time is
+the maximum over ranks.  Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (plain C, all host cores) on a bounded row
+sample of the same workload; the other ranks exit without work.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from int8_weight_quantized_gb300 import synthetic  # noqa: E402
+
+METRIC = "INT8 linear TOPS (2MNK/s, fused dequant) and % of GB300 dense INT8 peak"
+UNIT = "TOPS"
+WORKLOADS = {spec[0]: spec for spec in synthetic.ALL_WORKLOADS}
+DEFAULT_WORKLOAD = synthetic.TENSORWISE_4096[0]
+FLUSH_BYTES = 512 << 20  # > 129 MB of L2: written between steps (outside the timed events)
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+GEMM_SOURCES = ["int8_weight_quantized_gb300/csrc/gemm.cu", "int8_weight_quantized_gb300/csrc/ck_device.cuh"]
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def reduce_max(value, device="cpu"):
+    """Maximum of a float over all ranks (identity when not distributed)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    """(bf16 TFLOP/s burst, sustained, HBM GB/s, provenance)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def sources_sha256(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per GEMM launch from the committed ncu summary, or None when the
+    summary is missing, is for another workload, or predates the current kernel source."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)["gemm"]
+    except (OSError, KeyError, ValueError):
+        return None
+    if d.get("workload") != workload or d.get("source_sha256") != sources_sha256(GEMM_SOURCES):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock, power and throttle reasons while running."""
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.out = None
+        self.target = self._smi_id(device_index)
+
+    @staticmethod
+    def _smi_id(device_index):
+        try:
+            p = torch.cuda.get_device_properties(device_index)
+            return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:
+            return None
+
+    def start(self):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.target:
+            cmd[1:1] = ["-i", self.target]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        lines = self.out.read().splitlines()
+        self.out.close()
+        os.unlink(self.out.name)
+        return self.parse(lines)
+
+    @classmethod
+    def parse(cls, lines):
+        sm, mx, reasons = [], [], set()
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(cls.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(cls.REASONS, parts[5:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def workload_config(spec, l2_note):
+    name, M, N, K, mode, bias, frac, seed = spec
+    return {"workload": name, "M": M, "N": N, "K": K, "mode": synthetic.MODE_NAMES[mode], "bias": bool(bias),
+            "seed": seed, "l2": l2_note}
+
+
+# ---------------------------------------------------------------- the CPU oracle arms
+def oracle_step_rows(case, rows):
+    """One oracle evaluation of the layer on the first `rows` rows (its own scale for
+    tensorwise mode: the sample is the tensor)."""
+    import numpy as np
+    import oracle
+
+    x = case.x[:rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    if case.mode == synthetic.CONVROT:
+        w, ws = case.meta["w_rot"]
+    else:
+        w, ws = case.w.numpy(), case.w_scale.numpy()
+    b = None if case.bias is None else case.bias.contiguous().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.int8_linear(x, w, ws, b, mode=case.mode)
+    return time.perf_counter() - t0
+
+
+def prepare_oracle_case(spec):
+    case = synthetic.case_from_spec(spec)
+    if case.mode == synthetic.CONVROT:
+        import oracle
+        case.meta["w_rot"] = oracle.prepare_convrot_weight(case.w_float.numpy())
+    return case
+
+
+def cpu_baseline(spec, budget_s=12.0):
+    """The oracle as it stands, on a bounded row sample of the workload."""
+    import oracle
+
+    case = prepare_oracle_case(spec)
+    M, N, K = case.M, case.N, case.K
+    probe = min(M, max(8, oracle.num_threads()))
+    t = oracle_step_rows(case, probe)
+    rows = int(min(M, max(probe, probe * budget_s / max(t, 1e-6))))
+    t = oracle_step_rows(case, rows)
+    return {"value": 2.0 * rows * N * K / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "first %d of %d rows x all %d columns, K=%d (%.1f s)" % (rows, M, N, K, t)}
+
+
+def run_reference(args, spec):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    case = prepare_oracle_case(spec)
+    M, N, K = case.M, case.N, case.K
+    budget = 150.0  # seconds for warmup + timed steps together
+    probe = min(M, max(4, oracle.num_threads()))
+    t_probe = oracle_step_rows(case, probe)
+    per_row = t_probe / probe
+    rows = int(max(1, min(M, budget / (args.steps + args.warmup) / per_row)))
+    for _ in range(args.warmup):
+        oracle_step_rows(case, rows)
+    times = [oracle_step_rows(case, rows) for _ in range(args.steps)]
+    step_s = sum(times) / len(times)
+    value = 2.0 * rows * N * K / step_s / 1e12
+    sample = "first %d of %d rows x all %d columns, K=%d, per step" % (rows, M, N, K)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": workload_config(spec, "n/a (host)"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- the GPU arm
+def run_ours(args, spec):
+    import int8_weight_quantized_gb300 as ck
+    from int8_weight_quantized_gb300 import build as ck_build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    ck_build.build()
+    dev = torch.device("cuda", local)
+
+    name, M, N, K, mode, has_bias, frac, seed = spec
+    case = synthetic.case_from_spec(spec)
+    if mode == synthetic.CONVROT:
+        raise SystemExit("the ConvRot workload needs its pre-rotated weight from the oracle; bench the "
+                         "per-row or tensorwise workloads")
+    x = case.x.to(dev)
+    w = case.w.to(dev)
+    ws_ = case.w_scale.to(dev)
+    b = None if case.bias is None else case.bias.to(dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    work = ck.workspace(ck.ck_int8_linear_workspace_size(M, N, K, mode), dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ops = 2.0 * M * N * K
+
+    def step():
+        ck.ck_int8_linear(x, w, ws_, b, mode=mode, y=y, ws=work)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    if ck.ck_device_error(clear=True) != 0:
+        raise SystemExit("a kernel reported a wait timeout during warm-up")
+
+    # ---- timed region: K steps, device-resident inputs, L2 flushed between steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    ck.ck_profile_begin()
+    wall0 = time.perf_counter()
+    for i, (e0, e1) in enumerate(evs):
+        flush.fill_(i & 0xFF)
+        e0.record()
+        step()
+        e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier()
+    prof = ck.ck_profile_end()
+    clocks = sampler.stop()
+    step_ms_local = sum(a.elapsed_time(b_) for a, b_ in evs) / args.steps
+    step_ms = reduce_max(step_ms_local, dev)
+    value = world * ops / (step_ms * 1e-3) / 1e12
+    if ck.ck_device_error(clear=True) != 0:
+        raise SystemExit("a kernel reported a wait timeout in the timed region")
+
+    # ---- roofline of the dominant kernel (the GEMM) and the bandwidth-bound ones
+    bf16_peak, bf16_sust, hbm_peak, provenance = load_peaks()
+    g_ms, g_n = prof["gemm"]
+    q_ms, q_n = prof["quantize"]
+    w_ms, w_n = prof["widen"]
+    gemm_avg_ms = g_ms / max(g_n, 1)
+    achieved = ops / (gemm_avg_ms * 1e-3) / 1e12
+    traffic = profiled_traffic(name)
+    quant_bytes = (3 if mode == synthetic.TENSORWISE else 2) * 2 * M * K + 4 * M  # reads of x (2 B) + bf16 codes (2 B)
+    widen_bytes = 3 * N * K
+    q_steps = max(q_ms, 1e-9) / args.steps
+    w_steps = max(w_ms, 1e-9) / args.steps
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": achieved / bf16_peak, "traffic": traffic,
+                "kernel": "gemm_kernel (tcgen05 kind::f16 on int8 codes, exact int32, fused dequant)",
+                "peak_source": "%s bf16 dense (burst); sustained %.1f" % (provenance, bf16_sust),
+                "avg_launch_ms": gemm_avg_ms}
+    kernels = {
+        "gemm": {"ms_per_step": g_ms / args.steps, "launches": g_n},
+        "quantize": {"ms_per_step": q_steps, "launches": q_n, "GB/s": quant_bytes / (q_steps * 1e-3) / 1e9,
+                     "frac_hbm": quant_bytes / (q_steps * 1e-3) / 1e9 / hbm_peak},
+        "widen": {"ms_per_step": w_steps, "launches": w_n, "GB/s": widen_bytes / (w_steps * 1e-3) / 1e9,
+                  "frac_hbm": widen_bytes / (w_steps * 1e-3) / 1e9 / hbm_peak},
+    }
+
+    # ---- end to end through the same call, from and to pinned host memory
+    e2e_steps = max(20, min(args.steps, 500))
+    x_host = case.x.pin_memory()
+    y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i, (e0, e1) in enumerate(e2e_evs):
+        flush.fill_(i & 0xFF)
+        e0.record()
+        x.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+        e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(sum(a.elapsed_time(b_) for a, b_ in e2e_evs) / e2e_steps, dev)
+    e2e = {"value": world * ops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,
+           "d2h_bytes_per_step": y_host.numel() * 2, "ms_per_step": e2e_ms}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": workload_config(spec, "flushed between steps (%d MiB write)" % (FLUSH_BYTES >> 20)),
+            "roofline": roofline, "kernels": kernels, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": int(g_n + q_n + w_n), "timed_wall_s": wall}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    spec = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, spec)
+    return run_ours(args, spec)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

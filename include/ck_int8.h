@@ -1,0 +1,151 @@
+/*
+ * ck_int8.h -- C ABI of the INT8 quantized linear layer for one NVIDIA GB300 (sm_103a).
+ *
+ *   y[m,n] = bf16( float(acc[m,n]) * x_scale[m] * w_scale[n] (+ bias[n]) )
+ *   acc[m,n] = sum_k q[m,k] * w[n,k]            exact int32
+ *   q = clamp(rint(v / x_scale), -127, 127),  x_scale = max|v| / 127
+ *   v = x (TENSORWISE, PER_ROW) or x @ H (CONVROT)
+ *
+ * Sources (comfy-kitchen pages):
+ *   - issue #280 "INT8 linears on sm_121 (GB10 / DGX Spark) run at ~37% of tensor-core
+ *     peak via cutlass_int8_dequant; a fused-dequant Triton GEMM reaches ~88%,
+ *     bit-identical", sections "Kernel used" (int32 accumulator over K; fp32 epilogue
+ *     acc * x_scale[m] * w_scale[n] (+ bias[n]) -> output dtype; int64 offsets) and
+ *     "Exactness" (same operation order; tensor-wide scales; no-bias calls);
+ *   - issue #278 "int8_linear silently falls back to a DP4A-emulated INT8 GEMM on Volta
+ *     (sm_70) ...", section "2. quantize_int8_rowwise raises instead of falling back"
+ *     (the per-row quantize op) and "Suggested fix" (ConvRot: stored weight
+ *     W_rot = W @ H^T, activation rotated online x_rot = x @ H, no inverse rotation);
+ *   - issue #136 "INT8 GEMM kernels index the output in int32: illegal memory access
+ *     once m*n >= 2**31", sections "Summary" and "Suggested fix" (64-bit addressing);
+ *     section "Minimal reproduction" gives the call int8_linear(x, w, ws, out_dtype)
+ *     with x bf16 [m,k], w int8 [n,k], ws fp32 [n].
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense row-major device buffers owned by the caller.  The library
+ *     keeps no pointer after a call returns and allocates no device memory per call.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *     runs asynchronously; no entry point synchronises the host except
+ *     ck_device_error() and ck_selftest_wait_timeout().
+ *   - Every entry point returns a ck_status_t.  On a non-OK status nothing was
+ *     enqueued (argument and device checks run first) unless the status is
+ *     CK_ERR_CUDA from a launch; ck_last_error() then describes the failure.
+ *   - Sizes are int64; every device address is computed in 64 bits, so M*N, M*K and
+ *     N*K may exceed 2^31.  Each single dimension must stay below 2^31 (tensor-copy
+ *     coordinates are 32-bit).
+ *   - Requirements (CK_ERR_INVALID_ARG otherwise): M, N, K >= 1; K % 16 == 0;
+ *     N % 8 == 0; K <= 131072 (so |acc| <= 127*127*K fits int32); every pointer
+ *     16-byte aligned; CONVROT needs K % 128 == 0.  M == 0 is accepted and does nothing
+ *     (after the shape checks); the buffers sized by M may then be NULL.
+ *   - Device: compute capability 10.3 (GB300) only, else CK_ERR_UNSUPPORTED_DEVICE.
+ *     There is no fallback path of any kind.
+ */
+#ifndef CK_INT8_H
+#define CK_INT8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CK_TENSORWISE = 0, /* one x_scale for the whole activation, one w_scale          */
+    CK_PER_ROW = 1,    /* x_scale per activation row, w_scale per output channel     */
+    CK_CONVROT = 2     /* like CK_PER_ROW on x @ H; w is the pre-rotated W @ H^T      */
+} ck_mode_t;
+
+typedef enum {
+    CK_OK = 0,
+    CK_ERR_INVALID_ARG = 1,
+    CK_ERR_UNSUPPORTED_DEVICE = 2,
+    CK_ERR_CUDA = 3,
+    CK_ERR_TIMEOUT = 4
+} ck_status_t;
+
+/* Per-row activation quantize (issue #278, quantize_int8_rowwise).
+ *   x:       bf16 [M,K] device, read only.
+ *   rotate:  0 = none; 1 = ConvRot, v = x @ H with H block-diagonal of the normalized
+ *            128x128 Sylvester Hadamard matrix (needs K % 128 == 0), evaluated as an
+ *            fp32 fast Walsh-Hadamard transform (spans 1..64 ascending, then times
+ *            fp32(1/sqrt(128))); v is never rounded to bf16.
+ *   q:       int8 [M,K] device, written: clamp(rint(v / x_scale[m]), -127, 127), rint
+ *            rounding half to even, v / x_scale one correctly rounded fp32 division.
+ *   x_scale: fp32 [M] device, written: max_k |v[m,k]| / 127 (fp32 division).  A row
+ *            whose scale is 0 gets q = 0. */
+int ck_quantize_int8_rowwise(const void *x, int64_t M, int64_t K, int rotate, int8_t *q, float *x_scale,
+                             void *stream);
+
+/* Tensorwise activation quantize (issue #280, "INT8 tensorwise linears"; tensor-wide
+ * scales): x_scale[0] = max_{m,k} |x| / 127, q as above with that single scale.
+ *   workspace: device scratch of at least ck_quantize_tensorwise_workspace_size()
+ *   bytes (per-block partial maxima); its content on entry does not matter. */
+size_t ck_quantize_tensorwise_workspace_size(void);
+int ck_quantize_int8_tensorwise(const void *x, int64_t M, int64_t K, int8_t *q, float *x_scale,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace ck_int8_linear needs for this problem (>= 0).  The
+ * workspace holds the quantized activation and the weight as bf16 integers (the
+ * tensor-core operand format), the activation scales and the tensorwise partial maxima. */
+size_t ck_int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
+
+/* The INT8 linear layer (issue #136 repro API int8_linear(x, w, ws, out_dtype) with
+ * the optional bias of issue #280):
+ *   x:       bf16 [M,K] activations, device.
+ *   w:       int8 [N,K] weights, device; values in [-127, 127].  For CK_CONVROT this is
+ *            the pre-rotated, per-row quantized W @ H^T, used as is.
+ *   w_scale: fp32 [N] (CK_PER_ROW, CK_CONVROT) or fp32 [1] (CK_TENSORWISE).
+ *   bias:    bf16 [N] or NULL.
+ *   y:       bf16 [M,N], written.  y = bf16_rne(((float(acc) * xs) * ws) + bias) with
+ *            every fp32 operation rounded separately, in that order.
+ *   workspace/workspace_bytes: device scratch of ck_int8_linear_workspace_size() bytes.
+ * No int32 intermediate is ever written to device memory. */
+int ck_int8_linear(const void *x, const int8_t *w, const float *w_scale, const void *bias, void *y, int64_t M,
+                   int64_t N, int64_t K, int mode, void *workspace, size_t workspace_bytes, void *stream);
+
+/* GEMM + fused dequant on an already-quantized activation (the second half of
+ * ck_int8_linear): q int8 [M,K], x_scale fp32 [M] (or [1] if scalar_scales), w int8
+ * [N,K], w_scale fp32 [N] (or [1]), bias bf16 [N] or NULL, y bf16 [M,N].
+ * workspace: ck_int8_gemm_workspace_size(M, N, K) bytes. */
+size_t ck_int8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+int ck_int8_gemm_dequant(const int8_t *q, const float *x_scale, const int8_t *w, const float *w_scale,
+                         const void *bias, void *y, int64_t M, int64_t N, int64_t K, int scalar_scales,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* The raw int32 accumulators acc[m,n] = sum_k q[m,k] w[n,k] of the same GEMM engine,
+ * written to acc int32 [M,N] (for exactness checks; the fused path never writes them).
+ * workspace: ck_int8_gemm_workspace_size(M, N, K) bytes. */
+int ck_int8_gemm_s32(const int8_t *q, const int8_t *w, int32_t *acc, int64_t M, int64_t N, int64_t K,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Launch profiling, for benchmarks.  Between ck_profile_begin() and ck_profile_end()
+ * every kernel this library enqueues from the calling host thread is bracketed by two
+ * CUDA events recorded on the kernel's own stream (the kernels themselves are
+ * unchanged).  ck_profile_end() waits for those events and fills, for each kernel kind
+ * k < nkinds (0 = activation quantize, 1 = int8 -> bf16 operand widening, 2 = GEMM with
+ * fused epilogue), ms[k] = summed device milliseconds and launches[k] = number of
+ * kernel launches.  Both arrays are host memory owned by the caller. */
+int ck_profile_begin(void);
+int ck_profile_end(double *ms, int64_t *launches, int nkinds);
+
+/* Text of the last non-OK status returned on this host thread ("" if none). */
+const char *ck_last_error(void);
+
+/* Synchronises the current device, returns the device error word the kernels set
+ * when a bounded wait gave up (0 = none; bit meanings in the csrc sources) and, if
+ * `clear`, resets it.  Returns -1 if the word could not be read. */
+int ck_device_error(int clear);
+
+/* Failure-detection self-test: launches one block that waits on a barrier nothing
+ * will ever complete, with a wait limit of timeout_ns.  The wait gives up, records
+ * the error and the block exits normally; the call synchronises and returns
+ * CK_ERR_TIMEOUT when that happened as designed (and clears the bit), CK_OK if the
+ * wait unexpectedly completed, CK_ERR_CUDA on a CUDA error. */
+int ck_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CK_INT8_H */

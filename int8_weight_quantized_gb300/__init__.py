@@ -1,0 +1,220 @@
+"""INT8 quantized linear layer for one NVIDIA GB300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/ck_int8.h`` (library ``lib/libck_int8.so``,
+built by ``build.py``).  The functions have the C names and only marshal arguments:
+they check dtypes/shapes, allocate outputs with torch when the caller passes none,
+and hand raw device pointers plus the current CUDA stream to the library.  Every step
+of the computation runs in the library's CUDA kernels; if the library is missing or
+the device is not a GB300 the call raises -- there is no other implementation.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+TENSORWISE, PER_ROW, CONVROT = 0, 1, 2
+CK_OK, CK_ERR_INVALID_ARG, CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA, CK_ERR_TIMEOUT = range(5)
+STATUS_NAMES = {0: "CK_OK", 1: "CK_ERR_INVALID_ARG", 2: "CK_ERR_UNSUPPORTED_DEVICE", 3: "CK_ERR_CUDA",
+                4: "CK_ERR_TIMEOUT"}
+
+LIB_PATH = _build.LIB
+_lib = None
+
+
+class CkError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+def load_library(path=None):
+    """Load libck_int8.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError("libck_int8.so is not built (expected at %s); run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+    L = ctypes.CDLL(path)
+    P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "ck_quantize_int8_rowwise": ([P, I64, I64, I, P, P, P], I),
+        "ck_quantize_tensorwise_workspace_size": ([], SZ),
+        "ck_quantize_int8_tensorwise": ([P, I64, I64, P, P, P, SZ, P], I),
+        "ck_int8_linear_workspace_size": ([I64, I64, I64, I], SZ),
+        "ck_int8_linear": ([P, P, P, P, P, I64, I64, I64, I, P, SZ, P], I),
+        "ck_int8_gemm_workspace_size": ([I64, I64, I64], SZ),
+        "ck_int8_gemm_dequant": ([P, P, P, P, P, P, I64, I64, I64, I, P, SZ, P], I),
+        "ck_int8_gemm_s32": ([P, P, P, I64, I64, I64, P, SZ, P], I),
+        "ck_profile_begin": ([], I),
+        "ck_profile_end": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I], I),
+        "ck_last_error": ([], ctypes.c_char_p),
+        "ck_device_error": ([I], I),
+        "ck_selftest_wait_timeout": ([ctypes.c_uint64, P], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(status):
+    if status != CK_OK:
+        msg = load_library().ck_last_error()
+        raise CkError(status, msg.decode() if msg else "")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _req(t, dtype, shape, name):
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+
+
+_workspaces = {}
+
+
+def workspace(nbytes, device=None):
+    """A cached uint8 device buffer of at least nbytes (one per device)."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    buf = _workspaces.get(device)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+        _workspaces[device] = buf
+    return buf
+
+
+def ck_quantize_int8_rowwise(x, rotate=False, q=None, x_scale=None, stream=None):
+    """Per-row quantize of bf16 x [M,K]; returns (q int8 [M,K], x_scale fp32 [M])."""
+    M, K = x.shape
+    _req(x, torch.bfloat16, (M, K), "x")
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device) if q is None else q
+    x_scale = torch.empty((M,), dtype=torch.float32, device=x.device) if x_scale is None else x_scale
+    _req(q, torch.int8, (M, K), "q")
+    _req(x_scale, torch.float32, (M,), "x_scale")
+    _check(load_library().ck_quantize_int8_rowwise(_ptr(x), M, K, int(bool(rotate)), _ptr(q), _ptr(x_scale),
+                                                   _stream(stream)))
+    return q, x_scale
+
+
+def ck_quantize_int8_tensorwise(x, q=None, x_scale=None, ws=None, stream=None):
+    """Tensorwise quantize of bf16 x [M,K]; returns (q int8 [M,K], x_scale fp32 [1])."""
+    M, K = x.shape
+    _req(x, torch.bfloat16, (M, K), "x")
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device) if q is None else q
+    x_scale = torch.empty((1,), dtype=torch.float32, device=x.device) if x_scale is None else x_scale
+    _req(q, torch.int8, (M, K), "q")
+    _req(x_scale, torch.float32, (1,), "x_scale")
+    L = load_library()
+    need = L.ck_quantize_tensorwise_workspace_size()
+    ws = workspace(need, x.device) if ws is None else ws
+    _check(L.ck_quantize_int8_tensorwise(_ptr(x), M, K, _ptr(q), _ptr(x_scale), _ptr(ws), ws.numel(),
+                                         _stream(stream)))
+    return q, x_scale
+
+
+def ck_int8_linear_workspace_size(M, N, K, mode):
+    return load_library().ck_int8_linear_workspace_size(M, N, K, int(mode))
+
+
+def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stream=None):
+    """y [M,N] bf16 = dequant(int32 GEMM(quantize(x [@ H]), w)) (+ bias)."""
+    M, K = x.shape
+    N = w.shape[0]
+    _req(x, torch.bfloat16, (M, K), "x")
+    _req(w, torch.int8, (N, K), "w")
+    _req(w_scale, torch.float32, (1,) if mode == TENSORWISE else (N,), "w_scale")
+    if bias is not None:
+        _req(bias, torch.bfloat16, (N,), "bias")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _req(y, torch.bfloat16, (M, N), "y")
+    L = load_library()
+    need = L.ck_int8_linear_workspace_size(M, N, K, int(mode))
+    ws = workspace(need, x.device) if ws is None else ws
+    _check(L.ck_int8_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, int(mode), _ptr(ws),
+                            ws.numel(), _stream(stream)))
+    return y
+
+
+def ck_int8_gemm_dequant(q, x_scale, w, w_scale, bias=None, scalar_scales=False, y=None, ws=None, stream=None):
+    """GEMM + fused dequant on pre-quantized q int8 [M,K]; returns y bf16 [M,N]."""
+    M, K = q.shape
+    N = w.shape[0]
+    _req(q, torch.int8, (M, K), "q")
+    _req(w, torch.int8, (N, K), "w")
+    _req(x_scale, torch.float32, (1,) if scalar_scales else (M,), "x_scale")
+    _req(w_scale, torch.float32, (1,) if scalar_scales else (N,), "w_scale")
+    if bias is not None:
+        _req(bias, torch.bfloat16, (N,), "bias")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=q.device) if y is None else y
+    _req(y, torch.bfloat16, (M, N), "y")
+    L = load_library()
+    need = L.ck_int8_gemm_workspace_size(M, N, K)
+    ws = workspace(need, q.device) if ws is None else ws
+    _check(L.ck_int8_gemm_dequant(_ptr(q), _ptr(x_scale), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K,
+                                  int(bool(scalar_scales)), _ptr(ws), ws.numel(), _stream(stream)))
+    return y
+
+
+def ck_int8_gemm_s32(q, w, acc=None, ws=None, stream=None):
+    """Raw exact int32 accumulators acc [M,N] = q [M,K] . w [N,K]^T."""
+    M, K = q.shape
+    N = w.shape[0]
+    _req(q, torch.int8, (M, K), "q")
+    _req(w, torch.int8, (N, K), "w")
+    acc = torch.empty((M, N), dtype=torch.int32, device=q.device) if acc is None else acc
+    _req(acc, torch.int32, (M, N), "acc")
+    L = load_library()
+    need = L.ck_int8_gemm_workspace_size(M, N, K)
+    ws = workspace(need, q.device) if ws is None else ws
+    _check(L.ck_int8_gemm_s32(_ptr(q), _ptr(w), _ptr(acc), M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return acc
+
+
+def ck_last_error():
+    msg = load_library().ck_last_error()
+    return msg.decode() if msg else ""
+
+
+def ck_device_error(clear=True):
+    return load_library().ck_device_error(int(bool(clear)))
+
+
+def ck_selftest_wait_timeout(timeout_ns=1_000_000, stream=None):
+    """Returns the status code of the bounded-wait self-test (CK_ERR_TIMEOUT expected)."""
+    return load_library().ck_selftest_wait_timeout(int(timeout_ns), _stream(stream))
+
+
+PROFILE_KINDS = ("quantize", "widen", "gemm")
+
+
+def ck_profile_begin():
+    _check(load_library().ck_profile_begin())
+
+
+def ck_profile_end():
+    """Returns {kind: (device_ms, launches)} for the launches since ck_profile_begin()."""
+    n = len(PROFILE_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _check(load_library().ck_profile_end(ms, cnt, n))
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(PROFILE_KINDS)}

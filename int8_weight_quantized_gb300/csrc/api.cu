@@ -1,0 +1,523 @@
+// api.cu -- the extern "C" boundary declared in include/ck_int8.h: argument checks,
+// device check, workspace layout, and the launch sequence of each entry point.
+// Every entry point validates before it enqueues anything and never synchronises the
+// host (except the two diagnostics at the end).
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <set>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "ck_int8.h"
+#include "ck_internal.h"
+
+namespace ck {
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char* where)
+{
+    return fail(CK_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool aligned16(const void* p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v)
+{
+    return (v + kAlign - 1) & ~(kAlign - 1);
+}
+
+constexpr int64_t kMaxDim = 0x7FFFFFFF;  // tensor-copy coordinates are 32-bit
+constexpr int64_t kMaxK = 131072;        // 127*127*K must fit int32
+
+// Checks shared by the GEMM entry points.  Returns CK_OK or a status with the message set.
+int check_gemm_shape(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 0 || N <= 0 || K <= 0)
+        return fail(CK_ERR_INVALID_ARG, "M must be >= 0 and N, K >= 1 (got M=%lld N=%lld K=%lld)", (long long)M,
+                    (long long)N, (long long)K);
+    if (M > kMaxDim || N > kMaxDim)
+        return fail(CK_ERR_INVALID_ARG, "M and N must each be < 2^31 (got M=%lld N=%lld)", (long long)M,
+                    (long long)N);
+    if (K % 16 != 0)
+        return fail(CK_ERR_INVALID_ARG, "K must be a multiple of 16 (got %lld)", (long long)K);
+    if (K > kMaxK)
+        return fail(CK_ERR_INVALID_ARG, "K must be <= %lld so the int32 accumulator cannot overflow (got %lld)",
+                    (long long)kMaxK, (long long)K);
+    if (N % 8 != 0)
+        return fail(CK_ERR_INVALID_ARG, "N must be a multiple of 8 (got %lld)", (long long)N);
+    return CK_OK;
+}
+
+int check_device(DeviceInfo* dev)
+{
+    cudaError_t e = current_device(dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "querying the current device");
+    if (dev->major != 10 || dev->minor != 3)
+        return fail(CK_ERR_UNSUPPORTED_DEVICE,
+                    "this library is built for GB300 (compute capability 10.3); device %d is %d.%d", dev->device,
+                    dev->major, dev->minor);
+    return CK_OK;
+}
+
+#define CK_REQUIRE_PTR(p)                                                                       \
+    do {                                                                                        \
+        if ((p) == nullptr)                                                                     \
+            return fail(CK_ERR_INVALID_ARG, "%s must not be NULL", #p);                         \
+        if (!aligned16(p))                                                                      \
+            return fail(CK_ERR_INVALID_ARG, "%s must be 16-byte aligned", #p);                  \
+    } while (0)
+
+struct LinearWorkspace {
+    void* a16;        // bf16 [M,K]: quantized activation as tensor-core operand
+    void* b16;        // bf16 [N,K]: weight as tensor-core operand
+    float* xs;        // fp32 [M] or [1]
+    float* partials;  // tensorwise partial maxima
+};
+
+size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int mode, int nparts)
+{
+    return align_up((size_t)M * K * 2) + align_up((size_t)N * K * 2) +
+           align_up(sizeof(float) * (size_t)(mode == CK_TENSORWISE ? 1 : (M > 0 ? M : 1))) +
+           align_up(sizeof(float) * (size_t)nparts);
+}
+
+LinearWorkspace carve_linear(void* ws, int64_t M, int64_t N, int64_t K, int mode)
+{
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    LinearWorkspace w;
+    w.a16 = p;
+    p += align_up((size_t)M * K * 2);
+    w.b16 = p;
+    p += align_up((size_t)N * K * 2);
+    w.xs = reinterpret_cast<float*>(p);
+    p += align_up(sizeof(float) * (size_t)(mode == CK_TENSORWISE ? 1 : (M > 0 ? M : 1)));
+    w.partials = reinterpret_cast<float*>(p);
+    return w;
+}
+
+size_t gemm_ws_bytes(int64_t M, int64_t N, int64_t K)
+{
+    return align_up((size_t)M * K * 2) + align_up((size_t)N * K * 2);
+}
+
+const int kMaxPartials = 1024;
+
+// ---- launch profiling: events around each kernel launch while enabled -------------
+enum ProfKind { kProfQuantize = 0, kProfWiden = 1, kProfGemm = 2, kProfKinds = 3 };
+struct ProfRec {
+    int kind;
+    int launches;
+    cudaEvent_t a, b;
+};
+thread_local bool g_prof_on = false;
+thread_local std::vector<ProfRec> g_prof_recs;
+thread_local std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event()
+{
+    if (!g_prof_pool.empty()) {
+        cudaEvent_t e = g_prof_pool.back();
+        g_prof_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess)
+        return nullptr;
+    return e;
+}
+
+// Brackets the launches made in its lifetime with two events on `s` when profiling is on.
+struct ProfScope {
+    bool active = false;
+    ProfRec r{};
+    cudaStream_t s;
+    ProfScope(int kind, int launches, cudaStream_t st) : s(st)
+    {
+        if (!g_prof_on)
+            return;
+        r.kind = kind;
+        r.launches = launches;
+        r.a = prof_event();
+        r.b = prof_event();
+        active = r.a && r.b && cudaEventRecord(r.a, s) == cudaSuccess;
+    }
+    ~ProfScope()
+    {
+        if (active && cudaEventRecord(r.b, s) == cudaSuccess)
+            g_prof_recs.push_back(r);
+    }
+};
+
+}  // namespace
+
+cudaError_t current_device(DeviceInfo* info)
+{
+    static DeviceInfo cache[64];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && cache[dev].device == dev) {
+        *info = cache[dev];
+        return cudaSuccess;
+    }
+    DeviceInfo d;
+    d.device = dev;
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64)
+        cache[dev] = d;
+    *info = d;
+    return cudaSuccess;
+}
+
+void log_shape(const char* what, int64_t M, int64_t N, int64_t K, int mode, const char* engine)
+{
+    static const bool on = [] {
+        const char* v = std::getenv("CK_LOG");
+        return v && v[0] == '1';
+    }();
+    if (!on)
+        return;
+    static std::mutex mu;
+    static std::set<std::tuple<std::string, int64_t, int64_t, int64_t, int>> seen;
+    std::lock_guard<std::mutex> lock(mu);
+    if (seen.insert(std::make_tuple(std::string(what), M, N, K, mode)).second)
+        fprintf(stderr, "[ck] %s M=%lld N=%lld K=%lld mode=%d engine=%s\n", what, (long long)M, (long long)N,
+                (long long)K, mode, engine);
+}
+
+}  // namespace ck
+
+using namespace ck;
+
+extern "C" {
+
+const char* ck_last_error(void)
+{
+    return g_last_error.c_str();
+}
+
+int ck_quantize_int8_rowwise(const void* x, int64_t M, int64_t K, int rotate, int8_t* q, float* x_scale,
+                             void* stream)
+{
+    if (M < 0 || K <= 0)
+        return fail(CK_ERR_INVALID_ARG, "M must be >= 0 and K >= 1 (got M=%lld K=%lld)", (long long)M, (long long)K);
+    if (K % 16 != 0)
+        return fail(CK_ERR_INVALID_ARG, "K must be a multiple of 16 (got %lld)", (long long)K);
+    if (rotate != 0 && rotate != 1)
+        return fail(CK_ERR_INVALID_ARG, "rotate must be 0 or 1 (got %d)", rotate);
+    if (rotate && K % 128 != 0)
+        return fail(CK_ERR_INVALID_ARG, "the ConvRot rotation needs K % 128 == 0 (got %lld)", (long long)K);
+    if (M == 0)
+        return CK_OK;  // nothing to do; empty buffers may be NULL
+    CK_REQUIRE_PTR(x);
+    CK_REQUIRE_PTR(q);
+    CK_REQUIRE_PTR(x_scale);
+    DeviceInfo dev;
+    int st = check_device(&dev);
+    if (st != CK_OK)
+        return st;
+    log_shape("quantize_rowwise", M, 0, K, rotate ? CK_CONVROT : CK_PER_ROW, "rows-warp");
+    cudaError_t e;
+    {
+        ProfScope ps(kProfQuantize, 1, static_cast<cudaStream_t>(stream));
+        e = launch_quantize_rows(x, M, K, rotate != 0, q, nullptr, x_scale, dev, static_cast<cudaStream_t>(stream));
+    }
+    return e == cudaSuccess ? CK_OK : cuda_fail(e, "ck_quantize_int8_rowwise launch");
+}
+
+size_t ck_quantize_tensorwise_workspace_size(void)
+{
+    return sizeof(float) * kMaxPartials;
+}
+
+int ck_quantize_int8_tensorwise(const void* x, int64_t M, int64_t K, int8_t* q, float* x_scale, void* workspace,
+                                size_t workspace_bytes, void* stream)
+{
+    if (M < 0 || K <= 0)
+        return fail(CK_ERR_INVALID_ARG, "M must be >= 0 and K >= 1 (got M=%lld K=%lld)", (long long)M, (long long)K);
+    if (K % 16 != 0)
+        return fail(CK_ERR_INVALID_ARG, "K must be a multiple of 16 (got %lld)", (long long)K);
+    if (M == 0)
+        return CK_OK;  // no maximum to take and nothing to quantize
+    CK_REQUIRE_PTR(x);
+    CK_REQUIRE_PTR(q);
+    CK_REQUIRE_PTR(x_scale);
+    CK_REQUIRE_PTR(workspace);
+    if (workspace_bytes < ck_quantize_tensorwise_workspace_size())
+        return fail(CK_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes,
+                    ck_quantize_tensorwise_workspace_size());
+    DeviceInfo dev;
+    int st = check_device(&dev);
+    if (st != CK_OK)
+        return st;
+    log_shape("quantize_tensorwise", M, 0, K, CK_TENSORWISE, "flat-two-pass");
+    cudaError_t e;
+    {
+        ProfScope ps(kProfQuantize, 2, static_cast<cudaStream_t>(stream));
+        e = launch_quantize_tensorwise(x, M, K, q, nullptr, x_scale, static_cast<float*>(workspace), dev,
+                                       static_cast<cudaStream_t>(stream));
+    }
+    return e == cudaSuccess ? CK_OK : cuda_fail(e, "ck_quantize_int8_tensorwise launch");
+}
+
+size_t ck_int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return 0;
+    return linear_ws_bytes(M, N, K, mode, kMaxPartials);
+}
+
+int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const void* bias, void* y, int64_t M,
+                   int64_t N, int64_t K, int mode, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (mode != CK_TENSORWISE && mode != CK_PER_ROW && mode != CK_CONVROT)
+        return fail(CK_ERR_INVALID_ARG, "mode must be 0 (tensorwise), 1 (per-row) or 2 (ConvRot), got %d", mode);
+    int st = check_gemm_shape(M, N, K);
+    if (st != CK_OK)
+        return st;
+    if (mode == CK_CONVROT && K % 128 != 0)
+        return fail(CK_ERR_INVALID_ARG, "ConvRot needs K % 128 == 0 (got %lld)", (long long)K);
+    if (M == 0)
+        return CK_OK;  // empty batch: x and y may be NULL
+    CK_REQUIRE_PTR(x);
+    CK_REQUIRE_PTR(w);
+    CK_REQUIRE_PTR(w_scale);
+    CK_REQUIRE_PTR(y);
+    CK_REQUIRE_PTR(workspace);
+    if (bias != nullptr && !aligned16(bias))
+        return fail(CK_ERR_INVALID_ARG, "bias must be 16-byte aligned");
+    const size_t need = ck_int8_linear_workspace_size(M, N, K, mode);
+    if (workspace_bytes < need)
+        return fail(CK_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+    DeviceInfo dev;
+    if ((st = check_device(&dev)) != CK_OK)
+        return st;
+    if (M == 0)
+        return CK_OK;
+    log_shape("int8_linear", M, N, K, mode, "tcgen05-bf16-exact 128x256x64 s4");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    LinearWorkspace ws = carve_linear(workspace, M, N, K, mode);
+    cudaError_t e;
+    {
+        ProfScope ps(kProfQuantize, mode == CK_TENSORWISE ? 2 : 1, s);
+        if (mode == CK_TENSORWISE)
+            e = launch_quantize_tensorwise(x, M, K, nullptr, ws.a16, ws.xs, ws.partials, dev, s);
+        else
+            e = launch_quantize_rows(x, M, K, mode == CK_CONVROT, nullptr, ws.a16, ws.xs, dev, s);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "ck_int8_linear quantize launch");
+    {
+        ProfScope ps(kProfWiden, 1, s);
+        e = launch_widen_int8(w, ws.b16, N * K, dev, s);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "ck_int8_linear weight widening launch");
+    GemmProblem p;
+    p.a = ws.a16;
+    p.b = ws.b16;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.x_scale = ws.xs;
+    p.w_scale = w_scale;
+    p.bias = bias;
+    p.scalar_scales = mode == CK_TENSORWISE;
+    p.y = y;
+    std::string why;
+    {
+        ProfScope ps(kProfGemm, 1, s);
+        e = launch_gemm(p, dev, s, &why);
+    }
+    if (e != cudaSuccess)
+        return why.empty() ? cuda_fail(e, "ck_int8_linear GEMM launch") : fail(CK_ERR_CUDA, "%s", why.c_str());
+    return CK_OK;
+}
+
+size_t ck_int8_gemm_workspace_size(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return 0;
+    return gemm_ws_bytes(M, N, K);
+}
+
+static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, const float* w_scale, const void* bias,
+                      void* y, int32_t* acc, int64_t M, int64_t N, int64_t K, int scalar_scales, void* workspace,
+                      size_t workspace_bytes, void* stream, const char* name)
+{
+    int st = check_gemm_shape(M, N, K);
+    if (st != CK_OK)
+        return st;
+    if (M == 0)
+        return CK_OK;  // empty batch: q, x_scale, y / acc may be NULL
+    CK_REQUIRE_PTR(q);
+    CK_REQUIRE_PTR(w);
+    CK_REQUIRE_PTR(workspace);
+    if (acc == nullptr) {
+        CK_REQUIRE_PTR(x_scale);
+        CK_REQUIRE_PTR(w_scale);
+        CK_REQUIRE_PTR(y);
+        if (bias != nullptr && !aligned16(bias))
+            return fail(CK_ERR_INVALID_ARG, "bias must be 16-byte aligned");
+    } else {
+        CK_REQUIRE_PTR(acc);
+    }
+    const size_t need = gemm_ws_bytes(M, N, K);
+    if (workspace_bytes < need)
+        return fail(CK_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+    DeviceInfo dev;
+    if ((st = check_device(&dev)) != CK_OK)
+        return st;
+    if (M == 0)
+        return CK_OK;
+    log_shape(name, M, N, K, scalar_scales ? CK_TENSORWISE : CK_PER_ROW, "tcgen05-bf16-exact 128x256x64 s4");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* p8 = static_cast<uint8_t*>(workspace);
+    void* a16 = p8;
+    void* b16 = p8 + align_up((size_t)M * K * 2);
+    cudaError_t e;
+    {
+        ProfScope ps(kProfWiden, 2, s);
+        if ((e = launch_widen_int8(q, a16, M * K, dev, s)) == cudaSuccess)
+            e = launch_widen_int8(w, b16, N * K, dev, s);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "operand widening launch");
+    GemmProblem p;
+    p.a = a16;
+    p.b = b16;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.x_scale = x_scale;
+    p.w_scale = w_scale;
+    p.bias = bias;
+    p.scalar_scales = scalar_scales != 0;
+    p.y = acc ? nullptr : y;
+    p.acc = acc;
+    std::string why;
+    {
+        ProfScope ps(kProfGemm, 1, s);
+        e = launch_gemm(p, dev, s, &why);
+    }
+    if (e != cudaSuccess)
+        return why.empty() ? cuda_fail(e, "GEMM launch") : fail(CK_ERR_CUDA, "%s", why.c_str());
+    return CK_OK;
+}
+
+int ck_int8_gemm_dequant(const int8_t* q, const float* x_scale, const int8_t* w, const float* w_scale,
+                         const void* bias, void* y, int64_t M, int64_t N, int64_t K, int scalar_scales,
+                         void* workspace, size_t workspace_bytes, void* stream)
+{
+    return gemm_entry(q, x_scale, w, w_scale, bias, y, nullptr, M, N, K, scalar_scales, workspace, workspace_bytes,
+                      stream, "int8_gemm_dequant");
+}
+
+int ck_int8_gemm_s32(const int8_t* q, const int8_t* w, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                     void* workspace, size_t workspace_bytes, void* stream)
+{
+    return gemm_entry(q, nullptr, w, nullptr, nullptr, nullptr, acc, M, N, K, 0, workspace, workspace_bytes, stream,
+                      "int8_gemm_s32");
+}
+
+int ck_profile_begin(void)
+{
+    g_prof_on = true;
+    for (const ProfRec& r : g_prof_recs) {
+        g_prof_pool.push_back(r.a);
+        g_prof_pool.push_back(r.b);
+    }
+    g_prof_recs.clear();
+    return CK_OK;
+}
+
+int ck_profile_end(double* ms, int64_t* launches, int nkinds)
+{
+    g_prof_on = false;
+    if (nkinds < 0 || (nkinds > 0 && (ms == nullptr || launches == nullptr)))
+        return fail(CK_ERR_INVALID_ARG, "ck_profile_end needs ms[] and launches[] of nkinds entries");
+    for (int k = 0; k < nkinds; ++k) {
+        ms[k] = 0.0;
+        launches[k] = 0;
+    }
+    int status = CK_OK;
+    for (const ProfRec& r : g_prof_recs) {
+        float t = 0.0f;
+        cudaError_t e = cudaEventSynchronize(r.b);
+        if (e == cudaSuccess)
+            e = cudaEventElapsedTime(&t, r.a, r.b);
+        if (e != cudaSuccess && status == CK_OK)
+            status = cuda_fail(e, "reading profile events");
+        if (r.kind < nkinds) {
+            ms[r.kind] += t;
+            launches[r.kind] += r.launches;
+        }
+        g_prof_pool.push_back(r.a);
+        g_prof_pool.push_back(r.b);
+    }
+    g_prof_recs.clear();
+    return status;
+}
+
+int ck_device_error(int clear)
+{
+    unsigned int v = 0;
+    cudaError_t e = read_device_error(&v, clear != 0);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "reading the device error word");
+        return -1;
+    }
+    return (int)v;
+}
+
+int ck_selftest_wait_timeout(uint64_t timeout_ns, void* stream)
+{
+    DeviceInfo dev;
+    int st = check_device(&dev);
+    if (st != CK_OK)
+        return st;
+    unsigned int before = 0;
+    cudaError_t e = read_device_error(&before, true);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "clearing the device error word");
+    if ((e = launch_wait_selftest(timeout_ns, static_cast<cudaStream_t>(stream))) != cudaSuccess)
+        return cuda_fail(e, "wait self-test launch");
+    unsigned int after = 0;
+    if ((e = read_device_error(&after, true)) != cudaSuccess)
+        return cuda_fail(e, "wait self-test");
+    if (after & 16u)  // kErrWaitSelfTest
+        return fail(CK_ERR_TIMEOUT, "the self-test wait gave up after %llu ns, as designed",
+                    (unsigned long long)timeout_ns);
+    return CK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// ck_internal.h -- host-side interface between the C ABI (api.cu) and the kernels
+// (quantize.cu, gemm.cu).  Not installed; the public contract is include/ck_int8.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include <cuda_runtime.h>
+
+namespace ck {
+
+// One tensor-core GEMM problem: A [M,K] and B [N,K] are bf16 tensors whose values are
+// integers in [-127, 127] (the int8 codes, widened); the kernel forms the exact
+// integer products and either dequantizes them (y != nullptr) or writes the raw int32
+// accumulators (acc != nullptr).
+struct GemmProblem {
+    const void* a = nullptr;
+    const void* b = nullptr;
+    int64_t M = 0, N = 0, K = 0;
+    const float* x_scale = nullptr;
+    const float* w_scale = nullptr;
+    const void* bias = nullptr;  // bf16 [N] or nullptr
+    int scalar_scales = 0;
+    void* y = nullptr;           // bf16 [M,N]
+    int32_t* acc = nullptr;      // int32 [M,N]
+};
+
+struct DeviceInfo {
+    int device = -1;
+    int major = 0, minor = 0;
+    int sm_count = 0;
+};
+
+// Query (once per device) and return the current device's properties.
+cudaError_t current_device(DeviceInfo* info);
+
+// Kernel launchers.  Each returns cudaSuccess or the launch error; `why` gets a
+// description of a failure that is not a CUDA error.
+cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why);
+cudaError_t launch_quantize_rows(const void* x, int64_t M, int64_t K, bool rotate, int8_t* q8, void* q16,
+                                 float* x_scale, const DeviceInfo& dev, cudaStream_t s);
+// Tensorwise quantize in two launches: per-block maxima into `partials`
+// (tensorwise_partials() floats), then the quantize pass, which first reduces them.
+int tensorwise_partials(const DeviceInfo& dev);
+cudaError_t launch_quantize_tensorwise(const void* x, int64_t M, int64_t K, int8_t* q8, void* q16,
+                                       float* x_scale, float* partials, const DeviceInfo& dev, cudaStream_t s);
+// int8 -> bf16 widening of n values (n % 16 == 0).
+cudaError_t launch_widen_int8(const int8_t* src, void* dst, int64_t n, const DeviceInfo& dev, cudaStream_t s);
+
+// Device error word (bits in ck_device.cuh).
+cudaError_t read_device_error(unsigned int* value, bool clear);
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s);
+
+// Diagnostics: one line per unique problem shape when CK_LOG=1.
+void log_shape(const char* what, int64_t M, int64_t N, int64_t K, int mode, const char* engine);
+
+}  // namespace ck

@@ -1,0 +1,537 @@
+// gemm.cu -- exact INT8 x INT8 GEMM with the dequant epilogue fused, on the sm_103a
+// tensor cores (tcgen05), persistent and warp-specialised.
+//
+// What it computes (comfy-kitchen issue #280, "Kernel used" and "Exactness"):
+//   acc[m,n] = sum_k q[m,k] * w[n,k]   exactly (int32), then in fp32
+//   y[m,n]   = bf16( ((float(acc) * x_scale[m]) * w_scale[n]) + bias[n] )
+// with every address formed in 64 bits (issue #136, "Suggested fix").
+//
+// Engine.  sm_103a has no int8 tensor-core kind, so the int8 codes are fed to the
+// bf16 kind (kind::f16) as bf16 values: every integer in [-127, 127] is a bf16 exactly,
+// every product is an integer of magnitude <= 16129, and any partial sum of at most
+// 1024 such products has magnitude <= 16,516,096 < 2^24, so it is an exact fp32 integer.
+// The MMA therefore accumulates K in chunks of 1024 into an fp32 TMEM accumulator,
+// restarting the accumulator at each chunk; the epilogue warps convert each finished
+// chunk to int32 (exact) and add it to int32 running sums held in registers.  The
+// int32 sum is the true accumulator; it never leaves the SM.
+//
+// Roles (one CTA per SM, 10 warps):
+//   warp 0     TMA producer: A [128 x 64] and B [256 x 64] bf16 tiles per k-block into a
+//              4-stage ring of 128B-swizzled shared-memory buffers;
+//   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators) and issues
+//              tcgen05.mma (128x256x16) from one thread;
+//   warps 2-9  epilogue: warp w reads TMEM lanes 32*(w%4).. and one 128-column half;
+//              drains each chunk into its running sums, then dequantizes, converts to
+//              bf16, stages 32x32 boxes in shared memory and stores them with TMA.
+// The two accumulators ping-pong, so the MMA of the next chunk (or tile) overlaps the
+// drain and the store of the previous one.  Tiles are visited in a grouped order
+// (group_m tile-rows share a sweep over N) so concurrently resident tiles reuse A and
+// B from L2.  Every wait is bounded (see mbar_wait); a timed-out CTA records an error
+// bit, lets its copies and MMAs finish, frees TMEM and exits.
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "ck_device.cuh"
+#include "ck_internal.h"
+
+namespace ck {
+
+__device__ unsigned int g_device_error;
+
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;        // one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;    // K per kind::f16 instruction
+constexpr int STAGES = 4;
+constexpr int CHUNK_KB = 16;  // k-blocks per exact fp32 chunk (16 * 64 = 1024 products)
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 32 * (2 + EPI_WARPS);
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int OUT_COLS = 32;                                // columns per TMA store box
+constexpr uint32_t OUT_BUF_BYTES = 32 * OUT_COLS * 2;       // 32 rows x 64 bytes
+constexpr uint32_t OUT_BYTES = EPI_WARPS * 2 * OUT_BUF_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t BAR_BYTES = 256;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
+constexpr uint32_t IDESC = idesc_bf16_f32<BM, BN>();
+constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s per wait
+
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+
+struct Args {
+    int64_t M, N, K;
+    const float* xs;
+    const float* ws;
+    const __nv_bfloat16* bias;
+    int32_t* acc;
+    int64_t num_tiles;
+    int tiles_m, tiles_n, num_kb, group_m;
+    int scalar_scales;
+    uint64_t timeout_ns;
+};
+
+// Tile t -> (tile row, tile column) in grouped order.
+__device__ __forceinline__ void tile_coords(int64_t t, const Args& a, int& mb, int& nb)
+{
+    const int64_t per_group = (int64_t)a.group_m * a.tiles_n;
+    const int64_t g = t / per_group;
+    const int64_t first = g * a.group_m;
+    const int64_t rows = min((int64_t)a.group_m, (int64_t)a.tiles_m - first);
+    const int64_t r = t - g * per_group;
+    mb = (int)(first + r % rows);
+    nb = (int)(r / rows);
+}
+
+// Bounded wait used during teardown only (never raises the abort flag again).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                           uint64_t timeout_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity))
+            return;
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
+            atomicOr(err, kErrWaitDrain);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <bool RAW>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmY, const Args args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* s_ab = smem;
+    uint8_t* s_out = smem + (size_t)STAGES * STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_out + OUT_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* acc_full = bars + 2 * STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    unsigned int* err = &g_device_error;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (!RAW)
+            tma_prefetch_desc(&tmY);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0;       // stages holding a load
+            uint32_t issued_parity = 0;     // parity of that load's phase, per stage
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, args, mb, nb);
+                const int32_t m0 = mb * BM, n0 = nb * BN;
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kErrWaitProducer, args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = s_ab + (size_t)stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
+                    tma_load_2d(sa + A_BYTES, &tmB, &full[stage], kb * BK, n0);
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // the CTA is aborting: let every issued copy land before shared memory is released
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s))
+                        drain_wait(&full[s], (issued_parity >> s) & 1u, err, args.timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t acc_iter = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+                for (int kb0 = 0; kb0 < args.num_kb; kb0 += CHUNK_KB) {
+                    const uint32_t buf = acc_iter & 1u;
+                    const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                    if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort_flag, err, kErrWaitMma, args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    const int kend = min(kb0 + CHUNK_KB, args.num_kb);
+                    for (int kb = kb0; kb < kend; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, abort_flag, err, kErrWaitMma, args.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(s_ab + (size_t)stage * STAGE_BYTES);
+                        const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            // +32 bytes per 16-element K step inside the 128-byte swizzle row
+                            mma_bf16(d_tmem, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), IDESC,
+                                     (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&empty[stage]);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    mma_commit(&acc_full[buf]);
+                    ++acc_iter;
+                }
+            }
+            // every MMA issued above must be complete before TMEM is released
+            mma_commit(drain);
+            drain_wait(drain, 0, err, args.timeout_ns);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int e = warp - 2;
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int half = e >> 2;       // which 128 of the 256 tile columns
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        uint8_t* obuf = s_out + (size_t)e * 2 * OUT_BUF_BYTES;
+        uint32_t acc_iter = 0;
+        uint32_t nstore = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+            int mb, nb;
+            tile_coords(t, args, mb, nb);
+            const int64_t m0 = (int64_t)mb * BM;
+            const int64_t n0 = (int64_t)nb * BN;
+            int32_t run[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+                run[j] = 0;
+            for (int kb0 = 0; kb0 < args.num_kb; kb0 += CHUNK_KB) {
+                const uint32_t buf = acc_iter & 1u;
+                const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                // one lane polls, the warp follows its verdict (keeps the warp converged
+                // for the .sync.aligned TMEM loads)
+                int got = 1;
+                if (lane == 0)
+                    got = mbar_wait(&acc_full[buf], acc_phase, abort_flag, err, kErrWaitEpilogue, args.timeout_ns);
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + lane_base + buf * BN + half * 128;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + g * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        run[g * 32 + j] += __float2int_rz(__uint_as_float(v[j]));  // exact integer
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&acc_empty[buf]);
+                ++acc_iter;
+            }
+            if (!ok)
+                break;
+
+            const int64_t row = m0 + quarter * 32 + lane;
+            const int64_t cbase = n0 + half * 128;
+            if (RAW) {
+                if (row < args.M) {
+                    int32_t* dst = args.acc + row * args.N;
+#pragma unroll
+                    for (int c4 = 0; c4 < 32; ++c4) {
+                        const int64_t col = cbase + 4 * c4;
+                        if (col < args.N)  // N % 8 == 0: a 4-column group is all in or all out
+                            *reinterpret_cast<int4*>(dst + col) =
+                                make_int4(run[4 * c4], run[4 * c4 + 1], run[4 * c4 + 2], run[4 * c4 + 3]);
+                    }
+                }
+            } else {
+                const bool row_ok = row < args.M;
+                const float xsv = args.scalar_scales ? args.xs[0] : (row_ok ? args.xs[row] : 0.0f);
+                const int64_t row0 = m0 + quarter * 32;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const int64_t col0 = cbase + g * OUT_COLS;
+                    if (col0 >= args.N || row0 >= args.M)
+                        break;  // warp-uniform: nothing of this box is inside y
+                    uint8_t* buf = obuf + (nstore & 1u) * OUT_BUF_BYTES;
+                    if (lane == 0)
+                        bulk_wait_group_read<1>();  // the store that last used `buf` has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {  // 8 columns = one 16-byte chunk of the row
+                        const int64_t col = col0 + c * 8;
+                        float wsv[8], bv[8];
+                        if (col < args.N) {
+                            if (args.scalar_scales) {
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    wsv[i] = args.ws[0];
+                            } else {
+                                const float4 w0 = *reinterpret_cast<const float4*>(args.ws + col);
+                                const float4 w1 = *reinterpret_cast<const float4*>(args.ws + col + 4);
+                                wsv[0] = w0.x; wsv[1] = w0.y; wsv[2] = w0.z; wsv[3] = w0.w;
+                                wsv[4] = w1.x; wsv[5] = w1.y; wsv[6] = w1.z; wsv[7] = w1.w;
+                            }
+                            if (args.bias) {
+                                const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + col);
+                                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&braw);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    bv[2 * i] = __low2float(b2[i]);
+                                    bv[2 * i + 1] = __high2float(b2[i]);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                wsv[i] = 0.0f;
+                        }
+                        uint32_t packed[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float t0 = __int2float_rn(run[g * 32 + c * 8 + 2 * i]);
+                            float t1 = __int2float_rn(run[g * 32 + c * 8 + 2 * i + 1]);
+                            t0 = __fmul_rn(t0, xsv);
+                            t1 = __fmul_rn(t1, xsv);
+                            t0 = __fmul_rn(t0, wsv[2 * i]);
+                            t1 = __fmul_rn(t1, wsv[2 * i + 1]);
+                            if (args.bias) {
+                                t0 = __fadd_rn(t0, bv[2 * i]);
+                                t1 = __fadd_rn(t1, bv[2 * i + 1]);
+                            }
+                            packed[i] = pack_bf16x2(t0, t1);
+                        }
+                        // 64-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ ((r >> 1) & 3)
+                        const uint32_t phys = (uint32_t)c ^ (((uint32_t)lane >> 1) & 3u);
+                        *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) =
+                            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, buf, (int32_t)col0, (int32_t)row0);
+                        bulk_commit_group();
+                    }
+                    ++nstore;
+                }
+            }
+        }
+        if (lane == 0)
+            bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// The self-test of the bounded wait: one thread waits on a barrier that expects one
+// arrival that never comes.
+__global__ void wait_selftest_kernel(uint64_t timeout_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_wait(&bar, 0, &abort_flag, &g_device_error, kErrWaitSelfTest, timeout_ns);
+}
+
+}  // namespace gemm
+
+// ---------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor of `rows` x `cols` elements with a row pitch of `pitch_bytes`.
+static bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                        uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz,
+                        std::string* why)
+{
+    auto fn = encode_fn();
+    if (!fn) {
+        *why = "cuTensorMapEncodeTiled is not available from the driver";
+        return false;
+    }
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[160];
+        snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled failed (%d) for a %llux%llu tensor", (int)r,
+                 (unsigned long long)rows, (unsigned long long)cols);
+        *why = msg;
+        return false;
+    }
+    return true;
+}
+
+template <bool RAW>
+static cudaError_t ensure_smem_attr(int device)
+{
+    static bool done[64] = {};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    if (device >= 0 && device < 64 && done[device])
+        return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)gemm::SMEM_BYTES);
+    if (e == cudaSuccess && device >= 0 && device < 64)
+        done[device] = true;
+    return e;
+}
+
+cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why)
+{
+    using namespace gemm;
+    const bool raw = p.acc != nullptr;
+    CUtensorMap tmA, tmB, tmY;
+    if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, p.K, p.M, (uint64_t)p.K * 2, BK, BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B, why) ||
+        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.b, p.K, p.N, (uint64_t)p.K * 2, BK, BN,
+                     CU_TENSOR_MAP_SWIZZLE_128B, why))
+        return cudaErrorInvalidValue;
+    if (raw) {
+        tmY = tmA;  // unused by the raw-accumulator kernel
+    } else if (!make_map_2d(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.y, p.N, p.M, (uint64_t)p.N * 2, OUT_COLS, 32,
+                            CU_TENSOR_MAP_SWIZZLE_64B, why)) {
+        return cudaErrorInvalidValue;
+    }
+    Args a;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.xs = p.x_scale;
+    a.ws = p.w_scale;
+    a.bias = reinterpret_cast<const __nv_bfloat16*>(p.bias);
+    a.acc = p.acc;
+    a.tiles_m = (int)((p.M + BM - 1) / BM);
+    a.tiles_n = (int)((p.N + BN - 1) / BN);
+    a.num_tiles = (int64_t)a.tiles_m * a.tiles_n;
+    a.num_kb = (int)((p.K + BK - 1) / BK);
+    a.group_m = 8;
+    a.scalar_scales = p.scalar_scales;
+    a.timeout_ns = DEFAULT_TIMEOUT_NS;
+    const int grid = (int)std::min<int64_t>(a.num_tiles, dev.sm_count);
+    cudaError_t e = raw ? ensure_smem_attr<true>(dev.device) : ensure_smem_attr<false>(dev.device);
+    if (e != cudaSuccess)
+        return e;
+    if (raw)
+        gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmY, a);
+    else
+        gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmY, a);
+    return cudaGetLastError();
+}
+
+cudaError_t read_device_error(unsigned int* value, bool clear)
+{
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return e;
+    e = cudaMemcpyFromSymbol(value, g_device_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !clear)
+        return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+}
+
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s)
+{
+    gemm::wait_selftest_kernel<<<1, 32, 0, s>>>(timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace ck

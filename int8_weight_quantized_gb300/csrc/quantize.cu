@@ -1,0 +1,473 @@
+// quantize.cu -- activation quantize kernels (per-row, tensorwise, ConvRot-rotated)
+// and the int8 -> bf16 widening of tensor-core operands.  All are HBM-bandwidth bound:
+// 16-byte vector loads, warp-shuffle reductions, no shared-memory staging needed.
+//
+// What they compute (comfy-kitchen issue #278, quantize_int8_rowwise, and issue #280,
+// tensor-wide scales):
+//   x_scale = max|v| / 127 (fp32),  q = clamp(rint(v / x_scale), -127, 127)
+// with v = x, or v = x @ H for ConvRot (issue #278, "Suggested fix").
+//
+// Division.  rint(v / x_scale) must see the correctly rounded fp32 quotient.  When v
+// is a bf16 value (per-row and tensorwise modes) the row maximum is a bf16 value too,
+// and the quotient is formed from the correctly rounded reciprocal r = 1/s with one
+// FMA correction (Markstein, IBM J. Res. Dev. 34(1), 1990):
+//   t = v * r;  e = fma(-t, s, v)  (exact remainder);  t = fma(e, r, t)
+// which equals the IEEE quotient; this was checked exhaustively on the CPU for every
+// pair of bf16 significands (numerator <= maximum) over the full exponent range that
+// can reach rint's decision, with zero mismatches.  Rows with a tiny scale
+// (s < 2^-100) and every ConvRot row (fp32 v) use the IEEE division itself.
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ck_internal.h"
+
+namespace ck {
+namespace quant {
+
+constexpr int ROWS_PER_BLOCK = 8;  // one warp per row
+constexpr int THREADS = 32 * ROWS_PER_BLOCK;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// max |x| over the 8 bf16 values of a vector, on packed pairs (exact)
+__device__ __forceinline__ __nv_bfloat162 absmax8(__nv_bfloat162 m, const uint4& v)
+{
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        m = __hmax2(m, __habs2(p[i]));
+    return m;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8])
+{
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __low2float(p[i]);
+        f[2 * i + 1] = __high2float(p[i]);
+    }
+}
+
+// The per-element rule with scale s.  kind: 0 -> scale is zero (q = 0),
+// 1 -> reciprocal + Markstein correction, 2 -> IEEE division.
+struct Quantizer {
+    float s, r;
+    int kind;
+    __device__ __forceinline__ explicit Quantizer(float s_, bool exact_div_only)
+    {
+        s = s_;
+        r = 0.0f;
+        if (s_ == 0.0f) {
+            kind = 0;
+        } else if (!exact_div_only && s_ >= 0x1p-100f) {
+            kind = 1;
+            r = __fdiv_rn(1.0f, s_);
+        } else {
+            kind = 2;
+        }
+    }
+    __device__ __forceinline__ float operator()(float v) const
+    {
+        float t;
+        if (kind == 1) {
+            t = __fmul_rn(v, r);
+            const float e = __fmaf_rn(-t, s, v);
+            t = __fmaf_rn(e, r, t);
+        } else if (kind == 2) {
+            t = __fdiv_rn(v, s);
+        } else {
+            return 0.0f;
+        }
+        t = rintf(t);  // round half to even
+        return fminf(fmaxf(t, -127.0f), 127.0f);
+    }
+};
+
+template <bool OUT8, bool OUT16>
+__device__ __forceinline__ void store8(const float (&qv)[8], int8_t* q8, __nv_bfloat16* q16, int64_t off)
+{
+    if (OUT8) {
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo |= ((uint32_t)__float2int_rn(qv[i]) & 0xFFu) << (8 * i);
+            hi |= ((uint32_t)__float2int_rn(qv[4 + i]) & 0xFFu) << (8 * i);
+        }
+        *reinterpret_cast<uint2*>(q8 + off) = make_uint2(lo, hi);
+    }
+    if (OUT16) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(qv[2 * i], qv[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        *reinterpret_cast<uint4*>(q16 + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// ConvRot block transform of the 8 values a lane holds for one vector slot.  A
+// 128-block spans 16 lanes: element i = 8*(lane % 16) + e.  Spans 1, 2, 4 pair values
+// inside the thread, spans 8..64 pair lanes lane ^ 1..8.  (lo, hi) -> (lo + hi, lo - hi),
+// in ascending span order, then a multiply by fp32(1/sqrt(128)).
+__device__ __forceinline__ void fwht_slot(float (&v)[8], int lane)
+{
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if ((e & h) == 0) {
+                const float lo = v[e], hi = v[e + h];
+                v[e] = __fadd_rn(lo, hi);
+                v[e + h] = __fsub_rn(lo, hi);
+            }
+        }
+    }
+#pragma unroll
+    for (int hl = 1; hl < 16; hl <<= 1) {
+        const bool upper = (lane & hl) != 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float p = __shfl_xor_sync(0xffffffffu, v[e], hl);
+            v[e] = upper ? __fsub_rn(p, v[e]) : __fadd_rn(v[e], p);
+        }
+    }
+    const float c128 = 0.088388346f;  // fp32(1/sqrt(128)) = 0x3DB504F3
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        v[e] = __fmul_rn(v[e], c128);
+}
+
+// Per-row quantize with the row held in registers (K <= 256 * VPT).
+template <int VPT, bool OUT8, bool OUT16>
+__global__ void __launch_bounds__(THREADS) rows_plain_kernel(const uint4* __restrict__ x, int64_t M, int64_t K,
+                                                             int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
+                                                             float* __restrict__ xs)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
+    if (row >= M)
+        return;
+    const int64_t nvec = K >> 3;
+    const uint4* xr = x + row * nvec;
+    uint4 raw[VPT];
+    __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t idx = lane + 32 * j;
+        raw[j] = (idx < nvec) ? ld_stream(xr + idx) : make_uint4(0, 0, 0, 0);
+        m2 = absmax8(m2, raw[j]);
+    }
+    const float amax = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (lane == 0)
+        xs[row] = s;
+    const Quantizer qz(s, false);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t idx = lane + 32 * j;
+        if (idx < nvec) {
+            float f[8], qv[8];
+            unpack8(raw[j], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                qv[i] = qz(f[i]);
+            store8<OUT8, OUT16>(qv, q8, q16, row * K + idx * 8);
+        }
+    }
+}
+
+// ConvRot per-row quantize with the rotated row held in registers (K <= 256 * VPT).
+template <int VPT, bool OUT8, bool OUT16>
+__global__ void __launch_bounds__(THREADS) rows_rot_kernel(const uint4* __restrict__ x, int64_t M, int64_t K,
+                                                           int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
+                                                           float* __restrict__ xs)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
+    if (row >= M)
+        return;
+    const int64_t nvec = K >> 3;
+    const uint4* xr = x + row * nvec;
+    float v[VPT][8];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t idx = lane + 32 * j;
+        const uint4 r = (idx < nvec) ? ld_stream(xr + idx) : make_uint4(0, 0, 0, 0);
+        unpack8(r, v[j]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        if (32 * j < nvec) {  // warp-uniform: slot j holds at least one block
+            fwht_slot(v[j], lane);
+            if (lane + 32 * j < nvec) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    amax = fmaxf(amax, fabsf(v[j][e]));
+            }
+        }
+    }
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (lane == 0)
+        xs[row] = s;
+    const Quantizer qz(s, true);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t idx = lane + 32 * j;
+        if (idx < nvec) {
+            float qv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                qv[i] = qz(v[j][i]);
+            store8<OUT8, OUT16>(qv, q8, q16, row * K + idx * 8);
+        }
+    }
+}
+
+// Per-row quantize for rows too long to keep in registers: pass 1 finds the maximum,
+// pass 2 re-reads (from L2) and quantizes.
+template <bool ROT, bool OUT8, bool OUT16>
+__global__ void __launch_bounds__(THREADS) rows_stream_kernel(const uint4* __restrict__ x, int64_t M, int64_t K,
+                                                              int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
+                                                              float* __restrict__ xs)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
+    if (row >= M)
+        return;
+    const int64_t nvec = K >> 3;
+    const uint4* xr = x + row * nvec;
+    float amax = 0.0f;
+    for (int64_t base = 0; base < nvec; base += 32) {
+        const int64_t idx = base + lane;
+        const uint4 r = (idx < nvec) ? xr[idx] : make_uint4(0, 0, 0, 0);
+        float f[8];
+        unpack8(r, f);
+        if (ROT)
+            fwht_slot(f, lane);
+        if (idx < nvec) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                amax = fmaxf(amax, fabsf(f[e]));
+        }
+    }
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (lane == 0)
+        xs[row] = s;
+    const Quantizer qz(s, ROT);
+    for (int64_t base = 0; base < nvec; base += 32) {
+        const int64_t idx = base + lane;
+        const uint4 r = (idx < nvec) ? ld_stream(xr + idx) : make_uint4(0, 0, 0, 0);
+        float f[8], qv[8];
+        unpack8(r, f);
+        if (ROT)
+            fwht_slot(f, lane);
+        if (idx < nvec) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                qv[i] = qz(f[i]);
+            store8<OUT8, OUT16>(qv, q8, q16, row * K + idx * 8);
+        }
+    }
+}
+
+// Tensorwise pass 1: per-block maximum of |x| over a grid-stride slice.
+__global__ void __launch_bounds__(256) amax_partials_kernel(const uint4* __restrict__ x, int64_t nvec,
+                                                            float* __restrict__ partials)
+{
+    __shared__ float red[8];
+    __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride)
+        m2 = absmax8(m2, ld_stream(x + i));
+    float m = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+        m = warp_max(m);
+        if (threadIdx.x == 0)
+            partials[blockIdx.x] = m;
+    }
+}
+
+// Tensorwise pass 2: every block reduces the partial maxima (a few KB, L2 resident),
+// forms the one scale, and quantizes its grid-stride slice.
+template <bool OUT8, bool OUT16>
+__global__ void __launch_bounds__(256) quant_flat_kernel(const uint4* __restrict__ x, int64_t nvec,
+                                                         const float* __restrict__ partials, int nparts,
+                                                         int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
+                                                         float* __restrict__ xs)
+{
+    __shared__ float red[8];
+    __shared__ float s_amax;
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < nparts; i += blockDim.x)
+        m = fmaxf(m, partials[i]);
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+        m = warp_max(m);
+        if (threadIdx.x == 0)
+            s_amax = m;
+    }
+    __syncthreads();
+    const float s = __fdiv_rn(s_amax, 127.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        xs[0] = s;
+    const Quantizer qz(s, false);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        float f[8], qv[8];
+        unpack8(x[i], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            qv[e] = qz(f[e]);
+        store8<OUT8, OUT16>(qv, q8, q16, i * 8);
+    }
+}
+
+// int8 -> bf16 (exact), 16 values per thread and step.
+__global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ src, int64_t n16,
+                                                    uint4* __restrict__ dst)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+        const uint4 v = ld_stream(src + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float a = (float)(int8_t)((w[k] >> (16 * h)) & 0xFFu);
+                const float b = (float)(int8_t)((w[k] >> (16 * h + 8)) & 0xFFu);
+                __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+                o[2 * k + h] = *reinterpret_cast<uint32_t*>(&p);
+            }
+        }
+        dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+}  // namespace quant
+
+namespace {
+
+template <bool OUT8, bool OUT16>
+cudaError_t rows_dispatch(const void* x, int64_t M, int64_t K, bool rotate, int8_t* q8, void* q16, float* xs,
+                          cudaStream_t s)
+{
+    using namespace quant;
+    const uint4* xv = static_cast<const uint4*>(x);
+    __nv_bfloat16* q16b = static_cast<__nv_bfloat16*>(q16);
+    const int64_t blocks64 = (M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
+    if (blocks64 > 0x7FFFFFFF)
+        return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)blocks64;
+    const int64_t slots = (K + 255) / 256;  // 16-byte vectors per lane
+#define CK_ROWS(KERNEL, V) KERNEL<V, OUT8, OUT16><<<grid, THREADS, 0, s>>>(xv, M, K, q8, q16b, xs)
+    if (!rotate) {
+        if (slots <= 1) CK_ROWS(rows_plain_kernel, 1);
+        else if (slots <= 2) CK_ROWS(rows_plain_kernel, 2);
+        else if (slots <= 4) CK_ROWS(rows_plain_kernel, 4);
+        else if (slots <= 8) CK_ROWS(rows_plain_kernel, 8);
+        else if (slots <= 12) CK_ROWS(rows_plain_kernel, 12);
+        else if (slots <= 16) CK_ROWS(rows_plain_kernel, 16);
+        else if (slots <= 24) CK_ROWS(rows_plain_kernel, 24);
+        else rows_stream_kernel<false, OUT8, OUT16><<<grid, THREADS, 0, s>>>(xv, M, K, q8, q16b, xs);
+    } else {
+        if (slots <= 1) CK_ROWS(rows_rot_kernel, 1);
+        else if (slots <= 2) CK_ROWS(rows_rot_kernel, 2);
+        else if (slots <= 4) CK_ROWS(rows_rot_kernel, 4);
+        else if (slots <= 8) CK_ROWS(rows_rot_kernel, 8);
+        else if (slots <= 12) CK_ROWS(rows_rot_kernel, 12);
+        else if (slots <= 16) CK_ROWS(rows_rot_kernel, 16);
+        else rows_stream_kernel<true, OUT8, OUT16><<<grid, THREADS, 0, s>>>(xv, M, K, q8, q16b, xs);
+    }
+#undef CK_ROWS
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_rows(const void* x, int64_t M, int64_t K, bool rotate, int8_t* q8, void* q16,
+                                 float* x_scale, const DeviceInfo& dev, cudaStream_t s)
+{
+    (void)dev;
+    if (M == 0)
+        return cudaSuccess;
+    if (q8 && q16)
+        return rows_dispatch<true, true>(x, M, K, rotate, q8, q16, x_scale, s);
+    if (q8)
+        return rows_dispatch<true, false>(x, M, K, rotate, q8, q16, x_scale, s);
+    return rows_dispatch<false, true>(x, M, K, rotate, q8, q16, x_scale, s);
+}
+
+int tensorwise_partials(const DeviceInfo& dev)
+{
+    int n = 4 * dev.sm_count;
+    return n < 1 ? 1 : (n > 1024 ? 1024 : n);
+}
+
+cudaError_t launch_quantize_tensorwise(const void* x, int64_t M, int64_t K, int8_t* q8, void* q16, float* x_scale,
+                                       float* partials, const DeviceInfo& dev, cudaStream_t s)
+{
+    using namespace quant;
+    const int64_t nvec = (M * K) >> 3;
+    const int nparts = tensorwise_partials(dev);
+    const uint4* xv = static_cast<const uint4*>(x);
+    __nv_bfloat16* q16b = static_cast<__nv_bfloat16*>(q16);
+    amax_partials_kernel<<<nparts, 256, 0, s>>>(xv, nvec, partials);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const int grid = 4 * dev.sm_count;
+    if (q8 && q16)
+        quant_flat_kernel<true, true><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
+    else if (q8)
+        quant_flat_kernel<true, false><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
+    else
+        quant_flat_kernel<false, true><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_widen_int8(const int8_t* src, void* dst, int64_t n, const DeviceInfo& dev, cudaStream_t s)
+{
+    const int64_t n16 = n >> 4;
+    if (n16 == 0)
+        return cudaSuccess;
+    int64_t want = (n16 + 255) / 256;
+    const int64_t cap = (int64_t)8 * dev.sm_count;
+    const int grid = (int)(want < cap ? want : cap);
+    quant::widen_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), n16, static_cast<uint4*>(dst));
+    return cudaGetLastError();
+}
+
+}  // namespace ck

@@ -1,0 +1,26 @@
+"""Shared test helpers: bf16 bit views and bf16 ulp distances."""
+import numpy as np
+import torch
+
+
+def bits(t):
+    """bf16 torch tensor (any device) -> uint16 numpy bit patterns."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def from_bits(b, device="cpu"):
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def bf16_ulp_distance(a_bits, b_bits):
+    """Distance in bf16 units in the last place (+0 and -0 are the same point)."""
+    def ordered(u):
+        u = u.astype(np.int32)
+        return np.where(u & 0x8000, -(u & 0x7FFF), u)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+# The floating-point tolerance of the fused epilogue: at most 1 bf16 ulp from the
+# oracle (the same fp32 operation order gives 0; the bound admits a different but
+# still correctly-rounded-per-step evaluation).
+MAX_ULP = 1

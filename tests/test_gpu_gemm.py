@@ -1,0 +1,81 @@
+"""GPU parity of the tensor-core GEMM: raw int32 accumulators bit-exact against the
+oracle (including adversarial inputs that stress the exact-fp32-chunk argument), and
+the fused dequant epilogue within 1 bf16 ulp of the oracle's."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import int8_weight_quantized_gb300 as ck
+from int8_weight_quantized_gb300 import synthetic
+from helpers import bits, bf16_ulp_distance, MAX_ULP
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def gpu_acc(q, w):
+    acc = ck.ck_int8_gemm_s32(q.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    return acc.cpu().numpy()
+
+
+# several tiles, ragged M/N/K tails, one and several 1024-wide K chunks
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (1, 8, 16), (129, 264, 80), (300, 520, 1040),
+                                   (128, 256, 2048), (1000, 776, 3088), (77, 1032, 5376)])
+def test_s32_parity(M, N, K):
+    q = synthetic.int8_uniform((M, K), seed=M + K)
+    w = synthetic.int8_uniform((N, K), seed=N + 7 * K)
+    ref = oracle.gemm_s32(q.numpy(), w.numpy())
+    got = gpu_acc(q, w)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, "%d mismatches, first at %s: %d vs %d" % (len(bad), bad[0], got[tuple(bad[0])],
+                                                                     ref[tuple(bad[0])])
+
+
+@pytest.mark.parametrize("K", [1024, 1040, 2048, 4096, 65536])
+def test_s32_extreme_magnitudes(K):
+    """All +127 x +127 reaches the largest chunk partial (16,516,096 < 2^24 per 1024);
+    [127]*1023 + [1] keeps an odd total near 2^24 (low-bit retention); alternating signs
+    cancel exactly."""
+    M, N = 130, 264
+    q = torch.full((M, K), 127, dtype=torch.int8)
+    q[1::4] = -127
+    q[2::4, ::2] = -127
+    q[3::4, 1023::1024] = 1
+    w = torch.full((N, K), 127, dtype=torch.int8)
+    w[1::2] = -127
+    w[2::8, 1023::1024] = 1
+    ref = oracle.gemm_s32(q.numpy(), w.numpy())
+    got = gpu_acc(q, w)
+    assert np.array_equal(got, ref)
+    assert got[0, 0] == 127 * 127 * K
+
+
+def test_s32_int32_range_end():
+    """K = 131072 (the largest accepted): |acc| = 2,114,060,288, near the int32 limit."""
+    M, N, K = 128, 256, 131072
+    q = torch.full((M, K), 127, dtype=torch.int8)
+    q[1::2] = -127
+    w = torch.full((N, K), 127, dtype=torch.int8)
+    got = gpu_acc(q, w)
+    assert got[0, 0] == 127 * 127 * K and got[1, 0] == -127 * 127 * K
+    assert np.all(got[0::2] == 127 * 127 * K) and np.all(got[1::2] == -127 * 127 * K)
+
+
+@pytest.mark.parametrize("scalar", [False, True])
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (129, 264, 1040), (1, 8, 16)])
+def test_dequant_parity(M, N, K, scalar, with_bias):
+    q = synthetic.int8_uniform((M, K), seed=11 + M)
+    w = synthetic.int8_uniform((N, K), seed=12 + N)
+    xs = synthetic.scale_uniform(1 if scalar else M, seed=13, mul=0.02)
+    ws = synthetic.scale_uniform(1 if scalar else N, seed=14, mul=0.01)
+    b = synthetic.normal_bf16((1, N), seed=15, std=0.5).reshape(N) if with_bias else None
+    acc = oracle.gemm_s32(q.numpy(), w.numpy())
+    ref = oracle.dequant(acc, xs.numpy(), ws.numpy(), None if b is None else bits(b), scalar_scales=scalar)
+    y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), None if b is None else b.to(DEV),
+                                scalar_scales=scalar)
+    torch.cuda.synchronize()
+    d = bf16_ulp_distance(bits(y), ref)
+    assert d.max() <= MAX_ULP, "max ulp %d at %s" % (d.max(), np.unravel_index(d.argmax(), d.shape))

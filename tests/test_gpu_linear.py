@@ -1,0 +1,90 @@
+"""The whole layer, ck_int8_linear, on the workloads of the comfy-kitchen pages, against
+the CPU oracle: full outputs where the oracle finishes in seconds, seeded row samples
+(plus the first and last 16 rows) on the multi-GB shapes, including the M*N >= 2^31
+boundary of issue #136."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import int8_weight_quantized_gb300 as ck
+from int8_weight_quantized_gb300 import synthetic
+from helpers import bits, bf16_ulp_distance, MAX_ULP
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def convrot_weight(case):
+    w, ws = oracle.prepare_convrot_weight(case.w_float.cpu().numpy())
+    return torch.from_numpy(w), torch.from_numpy(ws)
+
+
+def run_full(spec):
+    case = synthetic.case_from_spec(spec)
+    if case.mode == synthetic.CONVROT:
+        w, ws = convrot_weight(case)
+    else:
+        w, ws = case.w, case.w_scale
+    b = case.bias
+    ref = oracle.int8_linear(bits(case.x), w.numpy(), ws.numpy(), None if b is None else bits(b), mode=case.mode)
+    y = ck.ck_int8_linear(case.x.to(DEV), w.to(DEV), ws.to(DEV), None if b is None else b.to(DEV), mode=case.mode)
+    torch.cuda.synchronize()
+    d = bf16_ulp_distance(bits(y), ref["y"])
+    assert d.max() <= MAX_ULP, "%s: max ulp %d at %s" % (spec[0], d.max(), np.unravel_index(d.argmax(), d.shape))
+    return case, y
+
+
+def test_per_row_256x512x512():
+    run_full(synthetic.PER_ROW_SMALL)
+
+
+def test_tensorwise_4096_cubed_with_bias():
+    run_full(synthetic.TENSORWISE_4096)
+
+
+def test_convrot_4096x12288x3072_with_bias():
+    case, y = run_full(synthetic.CONVROT_4096)
+    # the rotated layer stays close to the float layer it approximates
+    ref = case.x.float() @ case.w_float.T + case.bias.float()
+    rel = (y.float().cpu() - ref).norm() / ref.norm()
+    assert rel < 0.02
+
+
+@pytest.mark.parametrize("spec", synthetic.SWEEP[:2], ids=lambda s: s[0])
+def test_sweep_small_shapes_full(spec):
+    run_full(spec)
+
+
+def run_sampled(spec):
+    name, M, N, K, mode, bias, frac, seed = spec
+    # the activation is drawn on the GPU (multi-GB); the weight on the CPU, as the oracle needs all of it
+    x = synthetic.normal_bf16((M, K), seed, device=DEV)
+    w = synthetic.int8_uniform((N, K), seed + 101)
+    ws = synthetic.scale_uniform(N, seed + 202)
+    y = ck.ck_int8_linear(x, w.to(DEV), ws.to(DEV), None, mode=mode)
+    torch.cuda.synchronize()
+    rows = synthetic.sample_rows(M, seed=1000 + seed)
+    idx = torch.tensor(rows, device=DEV)
+    xr = bits(x.index_select(0, idx))
+    ref = oracle.int8_linear(xr, w.numpy(), ws.numpy(), None, mode=mode)
+    got = bits(y.index_select(0, idx))
+    d = bf16_ulp_distance(got, ref["y"])
+    assert d.max() <= MAX_ULP, "%s: max ulp %d at sample row %d" % (name, d.max(), rows[int(d.max(axis=1).argmax())])
+    # every row was written (no wrapped or skipped tile): finite values only
+    assert torch.isfinite(y[-1]).all() and torch.isfinite(y[0]).all()
+    del x, y
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("spec", synthetic.SWEEP[2:], ids=lambda s: s[0])
+def test_sweep_large_shapes_sampled(spec):
+    run_sampled(spec)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("spec", synthetic.LARGE_INDEX, ids=lambda s: s[0])
+def test_large_index_boundary_sampled(spec):
+    assert spec[1] * spec[2] >= 2 ** 31 - 21504  # straddles the int32 element-offset limit
+    run_sampled(spec)

@@ -1,0 +1,97 @@
+"""GPU parity of the activation quantize kernels against the CPU oracle: int8 codes and
+fp32 scales must be bit-identical (integer decisions taken in fp32 on both sides)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import int8_weight_quantized_gb300 as ck
+from int8_weight_quantized_gb300 import synthetic
+from helpers import bits, from_bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def check_rowwise(x_cpu, rotate):
+    q_ref, s_ref = oracle.quantize_rowwise(bits(x_cpu), rotate=rotate)
+    q, s = ck.ck_quantize_int8_rowwise(x_cpu.to(DEV), rotate=rotate)
+    torch.cuda.synchronize()
+    s_np = s.cpu().numpy()
+    assert np.array_equal(s_np.view(np.uint32), s_ref.view(np.uint32)), "x_scale differs"
+    qn = q.cpu().numpy()
+    bad = np.argwhere(qn != q_ref)
+    assert bad.size == 0, "q differs at %d places, first %s: gpu %d oracle %d" % (
+        len(bad), bad[0], qn[tuple(bad[0])], q_ref[tuple(bad[0])])
+
+
+# register-resident paths (K <= 6144), ragged tails of the 256-element lane slots, and
+# the two-pass path for long rows (K > 6144)
+@pytest.mark.parametrize("M,K", [(256, 512), (37, 16), (9, 48), (100, 2048), (3, 6144), (5, 5376),
+                                 (7, 6160), (2, 65536)])
+def test_rowwise_parity(M, K):
+    check_rowwise(synthetic.normal_bf16((M, K), seed=100 + K), rotate=False)
+
+
+@pytest.mark.parametrize("M,K", [(64, 128), (33, 384), (16, 4096), (3, 8192), (2, 4224)])
+def test_rowwise_convrot_parity(M, K):
+    oc = synthetic.outlier_columns(K, 0.01, seed=7)
+    check_rowwise(synthetic.normal_bf16((M, K), seed=200 + K, outlier_channels=oc), rotate=True)
+
+
+def test_convrot_workload_quantize_parity():
+    M, K = 4096, 3072
+    oc = synthetic.outlier_columns(K, 0.01, seed=5 + 404)
+    check_rowwise(synthetic.normal_bf16((M, K), seed=5, outlier_channels=oc), rotate=True)
+
+
+def test_exhaustive_bf16_significands():
+    """Every bf16 row maximum significand x every bf16 value below it (13 binades, both
+    signs): the reciprocal-and-correction quotient must round exactly like IEEE division."""
+    vals = []
+    for e in range(0, 13):
+        for m in range(128):
+            v = (1.0 + m / 128.0) * 2.0 ** (-e)
+            vals += [v, -v]
+    vals = np.array(vals, np.float64)
+    rows = []
+    for e_top in (0, 40, -60):
+        for m in range(128):
+            amax = (1.0 + m / 128.0) * 2.0 ** e_top
+            r = vals * 2.0 ** e_top
+            r = r[np.abs(r) <= amax]
+            row = np.zeros(3344, np.float64)
+            row[0] = amax
+            row[1:1 + len(r)] = r
+            rows.append(row)
+    x = torch.tensor(np.array(rows), dtype=torch.float32).to(torch.bfloat16)
+    assert torch.equal(x.float().double(), torch.tensor(np.array(rows)))  # all bf16-exact
+    check_rowwise(x, rotate=False)
+
+
+def test_zero_and_subnormal_rows():
+    x = synthetic.normal_bf16((6, 256), seed=3)
+    xb = bits(x).copy()
+    xb[0] = 0
+    xb[1] = 0x8000  # -0
+    xb[2] = np.array([0x0001, 0x8003, 0x0040, 0x0000] * 64, np.uint16)
+    xb[3, 1:] = 0
+    check_rowwise(from_bits(xb), rotate=False)
+    check_rowwise(from_bits(xb), rotate=True)
+
+
+@pytest.mark.parametrize("M,K", [(4096, 4096), (7, 48), (1, 16), (333, 1040)])
+def test_tensorwise_parity(M, K):
+    x = synthetic.normal_bf16((M, K), seed=300 + K)
+    q_ref, s_ref = oracle.quantize_tensorwise(bits(x))
+    q, s = ck.ck_quantize_int8_tensorwise(x.to(DEV))
+    torch.cuda.synchronize()
+    assert s.cpu().numpy().view(np.uint32)[0] == s_ref.view(np.uint32)[0]
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
+def test_empty_batch_is_a_no_op():
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    q, s = ck.ck_quantize_int8_rowwise(x)
+    torch.cuda.synchronize()
+    assert q.shape == (0, 64) and s.shape == (0,)
