@@ -85,6 +85,20 @@ size_t ck_quantize_tensorwise_workspace_size(void);
 int ck_quantize_int8_tensorwise(const void *x, int64_t M, int64_t K, int8_t *q, float *x_scale,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
+/* Tensorwise quantize for callers that cannot allocate device memory (code running
+ * under CUDA graph capture, fixed-budget real-time loops, hosts whose own allocator must
+ * own every byte).  No counterpart on the pages: it computes exactly what
+ * ck_quantize_int8_tensorwise computes, but keeps its partial maxima in a 16 KiB array
+ * built into the library (present on every GPU that loads it, until exit) instead of a
+ * caller workspace, and calls no allocation routine.
+ *   x, q, x_scale: as for ck_quantize_int8_tensorwise (caller-owned device buffers).
+ *   Limit: M*K <= 134,217,728 values, else CK_ERR_INVALID_ARG.
+ *   The first call on a device looks up the array's address there; make it before any
+ *   stream capture.  All calls share the array: calls that overlap on the GPU (other
+ *   streams or threads) race; serialize them. */
+int ck_quantize_int8_tensorwise_noalloc(const void *x, int64_t M, int64_t K, int8_t *q, float *x_scale,
+                                        void *stream);
+
 /* Bytes of device workspace ck_int8_linear needs for this problem (>= 0).  The
  * workspace holds the quantized activation and the weight as bf16 integers (the
  * tensor-core operand format), the activation scales and the tensorwise partial maxima. */

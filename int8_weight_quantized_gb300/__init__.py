@@ -44,6 +44,7 @@ def load_library(path=None):
         "ck_quantize_int8_rowwise": ([P, I64, I64, I, P, P, P], I),
         "ck_quantize_tensorwise_workspace_size": ([], SZ),
         "ck_quantize_int8_tensorwise": ([P, I64, I64, P, P, P, SZ, P], I),
+        "ck_quantize_int8_tensorwise_noalloc": ([P, I64, I64, P, P, P], I),
         "ck_int8_linear_workspace_size": ([I64, I64, I64, I], SZ),
         "ck_int8_linear": ([P, P, P, P, P, I64, I64, I64, I, P, SZ, P], I),
         "ck_int8_gemm_workspace_size": ([I64, I64, I64], SZ),
@@ -129,6 +130,18 @@ def ck_quantize_int8_tensorwise(x, q=None, x_scale=None, ws=None, stream=None):
     ws = workspace(need, x.device) if ws is None else ws
     _check(L.ck_quantize_int8_tensorwise(_ptr(x), M, K, _ptr(q), _ptr(x_scale), _ptr(ws), ws.numel(),
                                          _stream(stream)))
+    return q, x_scale
+
+
+def ck_quantize_int8_tensorwise_noalloc(x, q, x_scale, stream=None):
+    """Tensorwise quantize into caller-provided q int8 [M,K] and x_scale fp32 [1]; the
+    library allocates nothing (its partial maxima live in a fixed built-in array)."""
+    M, K = x.shape
+    _req(x, torch.bfloat16, (M, K), "x")
+    _req(q, torch.int8, (M, K), "q")
+    _req(x_scale, torch.float32, (1,), "x_scale")
+    _check(load_library().ck_quantize_int8_tensorwise_noalloc(_ptr(x), M, K, _ptr(q), _ptr(x_scale),
+                                                              _stream(stream)))
     return q, x_scale
 
 

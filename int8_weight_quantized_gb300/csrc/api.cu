@@ -521,3 +521,91 @@ int ck_selftest_wait_timeout(uint64_t timeout_ns, void* stream)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------
+// Tensorwise quantize without any allocation.
+//
+// Some callers cannot allocate device memory at all: code that runs while a CUDA graph
+// is being captured (cudaMalloc is not a capturable operation), real-time inference
+// loops that own a fixed memory budget and forbid allocator traffic, and hosts that
+// embed this library under another allocator which must see every byte.  They can
+// still pass their inputs and outputs, but not a workspace.  For them the partial
+// maxima of the tensorwise quantize live in a fixed array that is part of the loaded
+// module itself.
+//
+// Costs and limits, stated plainly:
+//   - the array holds kNoallocMaxPartials floats (16 KiB) on every GPU where this
+//     library's module is loaded, for the life of the process;
+//   - one partial maximum covers kNoallocValuesPerPartial input values, so M*K may be
+//     at most kNoallocMaxPartials * kNoallocValuesPerPartial = 134,217,728 values;
+//     larger tensors are rejected with CK_ERR_INVALID_ARG;
+//   - every call uses the same array.  Nothing in it needs to start at zero (each slot
+//     a call reads was written earlier by that same call), but two calls whose kernels
+//     overlap on the GPU -- different streams, or different host threads -- race on it
+//     and may return a wrong scale.  Serialize such calls on one stream;
+//   - the first call on a device looks up the array's device address on that device
+//     (cudaGetSymbolAddress, which also loads the module there).  Make that first call
+//     before any stream capture begins.
+namespace ck {
+namespace {
+
+constexpr int kNoallocMaxPartials = 4096;
+constexpr int64_t kNoallocVectorsPerPartial = 4096;  // 16-byte vectors of 8 bf16
+constexpr int64_t kNoallocValuesPerPartial = kNoallocVectorsPerPartial * 8;
+
+static __device__ __align__(256) float g_noalloc_partials[kNoallocMaxPartials];
+
+// Device address of g_noalloc_partials on the current device, looked up once per device.
+// (In host code the array's name is only a host-side stand-in, never a device address.)
+int noalloc_scratch(const DeviceInfo& dev, float** out)
+{
+    static std::mutex mu;
+    static float* addr[64] = {};
+    if (dev.device < 0 || dev.device >= 64)
+        return fail(CK_ERR_UNSUPPORTED_DEVICE, "device ordinal %d is out of range", dev.device);
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev.device] == nullptr) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_partials);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "looking up the no-allocation scratch array");
+        addr[dev.device] = static_cast<float*>(p);
+    }
+    *out = addr[dev.device];
+    return CK_OK;
+}
+
+}  // namespace
+}  // namespace ck
+
+extern "C" int ck_quantize_int8_tensorwise_noalloc(const void* x, int64_t M, int64_t K, int8_t* q, float* x_scale,
+                                                   void* stream)
+{
+    if (M < 0 || K <= 0)
+        return fail(CK_ERR_INVALID_ARG, "M must be >= 0 and K >= 1 (got M=%lld K=%lld)", (long long)M, (long long)K);
+    if (K % 16 != 0)
+        return fail(CK_ERR_INVALID_ARG, "K must be a multiple of 16 (got %lld)", (long long)K);
+    if (M > 0 && M > (kNoallocMaxPartials * kNoallocValuesPerPartial) / K)
+        return fail(CK_ERR_INVALID_ARG,
+                    "M*K = %lld exceeds the no-allocation limit of %lld values (%d partial maxima of %lld values); "
+                    "use ck_quantize_int8_tensorwise with a workspace",
+                    (long long)M * (long long)K, (long long)(kNoallocMaxPartials * kNoallocValuesPerPartial),
+                    kNoallocMaxPartials, (long long)kNoallocValuesPerPartial);
+    if (M == 0)
+        return CK_OK;
+    CK_REQUIRE_PTR(x);
+    CK_REQUIRE_PTR(q);
+    CK_REQUIRE_PTR(x_scale);
+    DeviceInfo dev;
+    int st = check_device(&dev);
+    if (st != CK_OK)
+        return st;
+    float* partials = nullptr;
+    if ((st = noalloc_scratch(dev, &partials)) != CK_OK)
+        return st;
+    const int64_t nvec = (M * K) >> 3;
+    const int nparts = (int)((nvec + kNoallocVectorsPerPartial - 1) / kNoallocVectorsPerPartial);
+    cudaError_t e = launch_quantize_tensorwise_parts(x, M, K, q, nullptr, x_scale, partials, nparts, dev,
+                                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CK_OK : cuda_fail(e, "ck_quantize_int8_tensorwise_noalloc launch");
+}

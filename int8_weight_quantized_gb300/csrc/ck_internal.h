@@ -45,6 +45,11 @@ cudaError_t launch_quantize_rows(const void* x, int64_t M, int64_t K, bool rotat
 int tensorwise_partials(const DeviceInfo& dev);
 cudaError_t launch_quantize_tensorwise(const void* x, int64_t M, int64_t K, int8_t* q8, void* q16,
                                        float* x_scale, float* partials, const DeviceInfo& dev, cudaStream_t s);
+// The same two launches with the number of partial maxima chosen by the caller
+// (`partials` holds at least nparts floats).
+cudaError_t launch_quantize_tensorwise_parts(const void* x, int64_t M, int64_t K, int8_t* q8, void* q16,
+                                             float* x_scale, float* partials, int nparts, const DeviceInfo& dev,
+                                             cudaStream_t s);
 // int8 -> bf16 widening of n values (n % 16 == 0).
 cudaError_t launch_widen_int8(const int8_t* src, void* dst, int64_t n, const DeviceInfo& dev, cudaStream_t s);
 

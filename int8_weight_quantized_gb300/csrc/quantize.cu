@@ -458,6 +458,28 @@ cudaError_t launch_quantize_tensorwise(const void* x, int64_t M, int64_t K, int8
     return cudaGetLastError();
 }
 
+cudaError_t launch_quantize_tensorwise_parts(const void* x, int64_t M, int64_t K, int8_t* q8, void* q16,
+                                             float* x_scale, float* partials, int nparts, const DeviceInfo& dev,
+                                             cudaStream_t s)
+{
+    using namespace quant;
+    const int64_t nvec = (M * K) >> 3;
+    const uint4* xv = static_cast<const uint4*>(x);
+    __nv_bfloat16* q16b = static_cast<__nv_bfloat16*>(q16);
+    amax_partials_kernel<<<nparts, 256, 0, s>>>(xv, nvec, partials);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const int grid = 4 * dev.sm_count;
+    if (q8 && q16)
+        quant_flat_kernel<true, true><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
+    else if (q8)
+        quant_flat_kernel<true, false><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
+    else
+        quant_flat_kernel<false, true><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_widen_int8(const int8_t* src, void* dst, int64_t n, const DeviceInfo& dev, cudaStream_t s)
 {
     const int64_t n16 = n >> 4;
