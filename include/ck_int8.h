@@ -134,13 +134,15 @@ int ck_int8_gemm_s32(const int8_t *q, const int8_t *w, int32_t *acc, int64_t M, 
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /* Launch profiling, for benchmarks.  Between ck_profile_begin() and ck_profile_end()
- * every kernel this library enqueues from the calling host thread is bracketed by two
- * CUDA events recorded on the kernel's own stream (the kernels themselves are
- * unchanged).  ck_profile_end() waits for those events and fills, for each kernel kind
- * k < nkinds (0 = activation quantize, 1 = int8 -> bf16 operand widening, 2 = GEMM with
- * fused epilogue), ms[k] = summed device milliseconds and launches[k] = number of
+ * the library counts the kernels it enqueues from the calling host thread, by kind
+ * (0 = activation quantize, 1 = int8 -> bf16 operand widening, 2 = GEMM with fused
+ * epilogue).  With with_events != 0 it also brackets each launch with two CUDA events on
+ * the kernel's own stream (the kernels are unchanged, but the events separate
+ * consecutive kernels, so launch overlap between them is lost while timing).
+ * ck_profile_end() waits for the events and fills, for each kind k < nkinds,
+ * ms[k] = summed device milliseconds (0 without events) and launches[k] = number of
  * kernel launches.  Both arrays are host memory owned by the caller. */
-int ck_profile_begin(void);
+int ck_profile_begin(int with_events);
 int ck_profile_end(double *ms, int64_t *launches, int nkinds);
 
 /* Text of the last non-OK status returned on this host thread ("" if none). */

@@ -50,7 +50,7 @@ def load_library(path=None):
         "ck_int8_gemm_workspace_size": ([I64, I64, I64], SZ),
         "ck_int8_gemm_dequant": ([P, P, P, P, P, P, I64, I64, I64, I, P, SZ, P], I),
         "ck_int8_gemm_s32": ([P, P, P, I64, I64, I64, P, SZ, P], I),
-        "ck_profile_begin": ([], I),
+        "ck_profile_begin": ([I], I),
         "ck_profile_end": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I], I),
         "ck_last_error": ([], ctypes.c_char_p),
         "ck_device_error": ([I], I),
@@ -220,8 +220,8 @@ def ck_selftest_wait_timeout(timeout_ns=1_000_000, stream=None):
 PROFILE_KINDS = ("quantize", "widen", "gemm")
 
 
-def ck_profile_begin():
-    _check(load_library().ck_profile_begin())
+def ck_profile_begin(with_events=True):
+    _check(load_library().ck_profile_begin(int(bool(with_events))))
 
 
 def ck_profile_end():

@@ -133,6 +133,8 @@ struct ProfRec {
     cudaEvent_t a, b;
 };
 thread_local bool g_prof_on = false;
+thread_local bool g_prof_events = false;
+thread_local int64_t g_prof_counts[kProfKinds] = {};
 thread_local std::vector<ProfRec> g_prof_recs;
 thread_local std::vector<cudaEvent_t> g_prof_pool;
 
@@ -157,6 +159,9 @@ struct ProfScope {
     ProfScope(int kind, int launches, cudaStream_t st) : s(st)
     {
         if (!g_prof_on)
+            return;
+        g_prof_counts[kind] += launches;
+        if (!g_prof_events)
             return;
         r.kind = kind;
         r.launches = launches;
@@ -449,9 +454,12 @@ int ck_int8_gemm_s32(const int8_t* q, const int8_t* w, int32_t* acc, int64_t M, 
                       "int8_gemm_s32");
 }
 
-int ck_profile_begin(void)
+int ck_profile_begin(int with_events)
 {
     g_prof_on = true;
+    g_prof_events = with_events != 0;
+    for (int k = 0; k < kProfKinds; ++k)
+        g_prof_counts[k] = 0;
     for (const ProfRec& r : g_prof_recs) {
         g_prof_pool.push_back(r.a);
         g_prof_pool.push_back(r.b);
@@ -467,7 +475,7 @@ int ck_profile_end(double* ms, int64_t* launches, int nkinds)
         return fail(CK_ERR_INVALID_ARG, "ck_profile_end needs ms[] and launches[] of nkinds entries");
     for (int k = 0; k < nkinds; ++k) {
         ms[k] = 0.0;
-        launches[k] = 0;
+        launches[k] = k < kProfKinds ? g_prof_counts[k] : 0;
     }
     int status = CK_OK;
     for (const ProfRec& r : g_prof_recs) {
@@ -477,10 +485,8 @@ int ck_profile_end(double* ms, int64_t* launches, int nkinds)
             e = cudaEventElapsedTime(&t, r.a, r.b);
         if (e != cudaSuccess && status == CK_OK)
             status = cuda_fail(e, "reading profile events");
-        if (r.kind < nkinds) {
+        if (r.kind < nkinds)
             ms[r.kind] += t;
-            launches[r.kind] += r.launches;
-        }
         g_prof_pool.push_back(r.a);
         g_prof_pool.push_back(r.b);
     }

@@ -30,6 +30,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while its
+// predecessor on the stream is still running; griddep_wait() blocks until that
+// predecessor has completed and its memory is visible.  Every kernel here calls it
+// before touching global memory.  griddep_launch_dependents() lets the successor launch
+// early (it still waits for this grid's completion in its own griddep_wait()).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 {

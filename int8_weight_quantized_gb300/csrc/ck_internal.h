@@ -5,10 +5,31 @@
 #include <cstddef>
 #include <cstdint>
 #include <string>
+#include <utility>
 
 #include <cuda_runtime.h>
 
 namespace ck {
+
+// Launch `kernel` with programmatic stream serialization, so its launch and prologue
+// overlap the tail of the previous kernel on the stream (the kernel itself calls
+// griddep_wait() before reading or writing global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // One tensor-core GEMM problem: A [M,K] and B [N,K] are bf16 tensors whose values are
 // integers in [-127, 127] (the int8 codes, widened); the kernel forms the exact

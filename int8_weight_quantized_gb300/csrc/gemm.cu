@@ -164,6 +164,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // everything above overlapped the previous kernel; from here on global memory is read
+    griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -391,6 +393,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     }
 
+    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -510,10 +513,8 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     if (e != cudaSuccess)
         return e;
     if (raw)
-        gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmY, a);
-    else
-        gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmY, a);
-    return cudaGetLastError();
+        return launch_pdl(gemm_kernel<true>, grid, THREADS, SMEM_BYTES, s, tmA, tmB, tmY, a);
+    return launch_pdl(gemm_kernel<false>, grid, THREADS, SMEM_BYTES, s, tmA, tmB, tmY, a);
 }
 
 cudaError_t read_device_error(unsigned int* value, bool clear)

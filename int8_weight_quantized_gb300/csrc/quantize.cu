@@ -21,6 +21,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "ck_device.cuh"
 #include "ck_internal.h"
 
 namespace ck {
@@ -28,6 +29,7 @@ namespace quant {
 
 constexpr int ROWS_PER_BLOCK = 8;  // one warp per row
 constexpr int THREADS = 32 * ROWS_PER_BLOCK;
+constexpr int UNROLL = 4;          // independent 16-byte loads in flight per thread in grid-stride loops
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p)
 {
@@ -162,6 +164,8 @@ __global__ void __launch_bounds__(THREADS) rows_plain_kernel(const uint4* __rest
                                                              int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
                                                              float* __restrict__ xs)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
     if (row >= M)
@@ -201,6 +205,8 @@ __global__ void __launch_bounds__(THREADS) rows_rot_kernel(const uint4* __restri
                                                            int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
                                                            float* __restrict__ xs)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
     if (row >= M)
@@ -251,6 +257,8 @@ __global__ void __launch_bounds__(THREADS) rows_stream_kernel(const uint4* __res
                                                               int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
                                                               float* __restrict__ xs)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
     if (row >= M)
@@ -296,11 +304,22 @@ __global__ void __launch_bounds__(THREADS) rows_stream_kernel(const uint4* __res
 __global__ void __launch_bounds__(256) amax_partials_kernel(const uint4* __restrict__ x, int64_t nvec,
                                                             float* __restrict__ partials)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ float red[8];
     __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride)
-        m2 = absmax8(m2, ld_stream(x + i));
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec; base += UNROLL * stride) {
+        uint4 v[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            v[u] = i < nvec ? ld_stream(x + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            m2 = absmax8(m2, v[u]);
+    }
     float m = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
     if ((threadIdx.x & 31) == 0)
         red[threadIdx.x >> 5] = m;
@@ -321,6 +340,8 @@ __global__ void __launch_bounds__(256) quant_flat_kernel(const uint4* __restrict
                                                          int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
                                                          float* __restrict__ xs)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ float red[8];
     __shared__ float s_amax;
     float m = 0.0f;
@@ -342,37 +363,70 @@ __global__ void __launch_bounds__(256) quant_flat_kernel(const uint4* __restrict
         xs[0] = s;
     const Quantizer qz(s, false);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-        float f[8], qv[8];
-        unpack8(x[i], f);
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec; base += UNROLL * stride) {
+        uint4 v[UNROLL];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            qv[e] = qz(f[e]);
-        store8<OUT8, OUT16>(qv, q8, q16, i * 8);
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            v[u] = i < nvec ? ld_stream(x + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            if (i < nvec) {
+                float f[8], qv[8];
+                unpack8(v[u], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    qv[e] = qz(f[e]);
+                store8<OUT8, OUT16>(qv, q8, q16, i * 8);
+            }
+        }
     }
 }
 
-// int8 -> bf16 (exact), 16 values per thread and step.
+// int8 -> bf16 (exact), 16 values per thread and vector.
+__device__ __forceinline__ void widen16(const uint4& v, uint4& lo, uint4& hi)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float a = (float)(int8_t)((w[k] >> (16 * h)) & 0xFFu);
+            const float b = (float)(int8_t)((w[k] >> (16 * h + 8)) & 0xFFu);
+            __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+            o[2 * k + h] = *reinterpret_cast<uint32_t*>(&p);
+        }
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ src, int64_t n16,
                                                     uint4* __restrict__ dst)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-        const uint4 v = ld_stream(src + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[8];
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < n16; base += UNROLL * stride) {
+        uint4 v[UNROLL];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            v[u] = i < n16 ? ld_stream(src + i) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float a = (float)(int8_t)((w[k] >> (16 * h)) & 0xFFu);
-                const float b = (float)(int8_t)((w[k] >> (16 * h + 8)) & 0xFFu);
-                __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
-                o[2 * k + h] = *reinterpret_cast<uint32_t*>(&p);
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            if (i < n16) {
+                uint4 lo, hi;
+                widen16(v[u], lo, hi);
+                dst[2 * i] = lo;
+                dst[2 * i + 1] = hi;
             }
         }
-        dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -392,7 +446,8 @@ cudaError_t rows_dispatch(const void* x, int64_t M, int64_t K, bool rotate, int8
         return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)blocks64;
     const int64_t slots = (K + 255) / 256;  // 16-byte vectors per lane
-#define CK_ROWS(KERNEL, V) KERNEL<V, OUT8, OUT16><<<grid, THREADS, 0, s>>>(xv, M, K, q8, q16b, xs)
+    cudaError_t e = cudaSuccess;
+#define CK_ROWS(KERNEL, V) e = launch_pdl(KERNEL<V, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs)
     if (!rotate) {
         if (slots <= 1) CK_ROWS(rows_plain_kernel, 1);
         else if (slots <= 2) CK_ROWS(rows_plain_kernel, 2);
@@ -401,7 +456,7 @@ cudaError_t rows_dispatch(const void* x, int64_t M, int64_t K, bool rotate, int8
         else if (slots <= 12) CK_ROWS(rows_plain_kernel, 12);
         else if (slots <= 16) CK_ROWS(rows_plain_kernel, 16);
         else if (slots <= 24) CK_ROWS(rows_plain_kernel, 24);
-        else rows_stream_kernel<false, OUT8, OUT16><<<grid, THREADS, 0, s>>>(xv, M, K, q8, q16b, xs);
+        else e = launch_pdl(rows_stream_kernel<false, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs);
     } else {
         if (slots <= 1) CK_ROWS(rows_rot_kernel, 1);
         else if (slots <= 2) CK_ROWS(rows_rot_kernel, 2);
@@ -409,10 +464,10 @@ cudaError_t rows_dispatch(const void* x, int64_t M, int64_t K, bool rotate, int8
         else if (slots <= 8) CK_ROWS(rows_rot_kernel, 8);
         else if (slots <= 12) CK_ROWS(rows_rot_kernel, 12);
         else if (slots <= 16) CK_ROWS(rows_rot_kernel, 16);
-        else rows_stream_kernel<true, OUT8, OUT16><<<grid, THREADS, 0, s>>>(xv, M, K, q8, q16b, xs);
+        else e = launch_pdl(rows_stream_kernel<true, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs);
     }
 #undef CK_ROWS
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace
@@ -444,18 +499,17 @@ cudaError_t launch_quantize_tensorwise(const void* x, int64_t M, int64_t K, int8
     const int nparts = tensorwise_partials(dev);
     const uint4* xv = static_cast<const uint4*>(x);
     __nv_bfloat16* q16b = static_cast<__nv_bfloat16*>(q16);
-    amax_partials_kernel<<<nparts, 256, 0, s>>>(xv, nvec, partials);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(amax_partials_kernel, nparts, 256, 0, s, xv, nvec, partials);
     if (e != cudaSuccess)
         return e;
     const int grid = 4 * dev.sm_count;
     if (q8 && q16)
-        quant_flat_kernel<true, true><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
+        e = launch_pdl(quant_flat_kernel<true, true>, grid, 256, 0, s, xv, nvec, partials, nparts, q8, q16b, x_scale);
     else if (q8)
-        quant_flat_kernel<true, false><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
+        e = launch_pdl(quant_flat_kernel<true, false>, grid, 256, 0, s, xv, nvec, partials, nparts, q8, q16b, x_scale);
     else
-        quant_flat_kernel<false, true><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
-    return cudaGetLastError();
+        e = launch_pdl(quant_flat_kernel<false, true>, grid, 256, 0, s, xv, nvec, partials, nparts, q8, q16b, x_scale);
+    return e;
 }
 
 cudaError_t launch_quantize_tensorwise_parts(const void* x, int64_t M, int64_t K, int8_t* q8, void* q16,
@@ -466,18 +520,17 @@ cudaError_t launch_quantize_tensorwise_parts(const void* x, int64_t M, int64_t K
     const int64_t nvec = (M * K) >> 3;
     const uint4* xv = static_cast<const uint4*>(x);
     __nv_bfloat16* q16b = static_cast<__nv_bfloat16*>(q16);
-    amax_partials_kernel<<<nparts, 256, 0, s>>>(xv, nvec, partials);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(amax_partials_kernel, nparts, 256, 0, s, xv, nvec, partials);
     if (e != cudaSuccess)
         return e;
     const int grid = 4 * dev.sm_count;
     if (q8 && q16)
-        quant_flat_kernel<true, true><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
+        e = launch_pdl(quant_flat_kernel<true, true>, grid, 256, 0, s, xv, nvec, partials, nparts, q8, q16b, x_scale);
     else if (q8)
-        quant_flat_kernel<true, false><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
+        e = launch_pdl(quant_flat_kernel<true, false>, grid, 256, 0, s, xv, nvec, partials, nparts, q8, q16b, x_scale);
     else
-        quant_flat_kernel<false, true><<<grid, 256, 0, s>>>(xv, nvec, partials, nparts, q8, q16b, x_scale);
-    return cudaGetLastError();
+        e = launch_pdl(quant_flat_kernel<false, true>, grid, 256, 0, s, xv, nvec, partials, nparts, q8, q16b, x_scale);
+    return e;
 }
 
 cudaError_t launch_widen_int8(const int8_t* src, void* dst, int64_t n, const DeviceInfo& dev, cudaStream_t s)
@@ -488,8 +541,8 @@ cudaError_t launch_widen_int8(const int8_t* src, void* dst, int64_t n, const Dev
     int64_t want = (n16 + 255) / 256;
     const int64_t cap = (int64_t)8 * dev.sm_count;
     const int grid = (int)(want < cap ? want : cap);
-    quant::widen_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), n16, static_cast<uint4*>(dst));
-    return cudaGetLastError();
+    return launch_pdl(quant::widen_kernel, grid, 256, 0, s, reinterpret_cast<const uint4*>(src), n16,
+                      static_cast<uint4*>(dst));
 }
 
 }  // namespace ck
