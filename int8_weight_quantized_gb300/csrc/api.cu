@@ -90,6 +90,8 @@ int check_device(DeviceInfo* dev)
             return fail(CK_ERR_INVALID_ARG, "%s must be 16-byte aligned", #p);                  \
     } while (0)
 
+constexpr int kMaxPartialsForLayout = 1024;  // tensorwise partial maxima region (floats)
+
 struct LinearWorkspace {
     void* a16;        // bf16 [M,K]: quantized activation as tensor-core operand
     void* b16;        // bf16 [N,K]: weight as tensor-core operand
@@ -123,7 +125,7 @@ size_t gemm_ws_bytes(int64_t M, int64_t N, int64_t K)
     return align_up((size_t)M * K * 2) + align_up((size_t)N * K * 2);
 }
 
-const int kMaxPartials = 1024;
+const int kMaxPartials = kMaxPartialsForLayout;
 
 // ---- launch profiling: events around each kernel launch while enabled -------------
 enum ProfKind { kProfQuantize = 0, kProfWiden = 1, kProfGemm = 2, kProfKinds = 3 };

@@ -15,21 +15,32 @@
 // chunk to int32 (exact) and add it to int32 running sums held in registers.  The
 // int32 sum is the true accumulator; it never leaves the SM.
 //
+// CTA pairs (the default when there are at least two 128-row tiles).  A 2-CTA cluster
+// computes a 256 x 256 tile with tcgen05 cta_group::2: each CTA holds 128 activation
+// rows and 128 of the 256 weight rows of every k-block in its own shared memory, the
+// leader CTA issues one 256x256x16 MMA that reads both CTAs' operands, and each CTA's
+// TMEM receives its own 128 output rows.  Per SM this halves the weight bytes that
+// shared memory must take in and hand to the tensor core, compared with one CTA per
+// 128 x 256 tile.  Problems with a single tile row run one CTA per 128 x 256 tile.
+//
 // Roles (one CTA per SM, 10 warps):
-//   warp 0     TMA producer: A [128 x 64] and B [256 x 64] bf16 tiles per k-block into a
-//              4-stage ring of 128B-swizzled shared-memory buffers;
-//   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators) and issues
-//              tcgen05.mma (128x256x16) from one thread;
+//   warp 0     TMA producer: this CTA's A [128 x 64] and B [128 x 64] (pair) or B [256 x 64]
+//              (single) bf16 boxes per k-block into a ring of 128B-swizzled stages; in a
+//              pair, completion is counted on the leader's barrier;
+//   warp 1     allocates 512 TMEM columns (two fp32 accumulators of 256 columns) and, in
+//              the leader (or single CTA), issues the MMAs from one thread;
 //   warps 2-9  epilogue: warp w reads TMEM lanes 32*(w%4).. and one 128-column half;
 //              drains each chunk into its running sums, then dequantizes, converts to
 //              bf16, stages 32x32 boxes in shared memory and stores them with TMA.
 // The two accumulators ping-pong, so the MMA of the next chunk (or tile) overlaps the
 // drain and the store of the previous one.  Tiles are visited in a grouped order
-// (group_m tile-rows share a sweep over N) so concurrently resident tiles reuse A and
-// B from L2.  Every wait is bounded (see mbar_wait); a timed-out CTA records an error
-// bit, lets its copies and MMAs finish, frees TMEM and exits.
+// (group_m unit rows share a sweep over N) so concurrently resident CTAs reuse operands
+// from L2.  Every wait is bounded (see mbar_wait); a timed-out CTA records an error bit,
+// lets its copies and MMAs finish, frees TMEM and exits.
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include <cuda.h>
@@ -46,28 +57,35 @@ __device__ unsigned int g_device_error;
 
 namespace gemm {
 
-constexpr int BM = 128;
+constexpr int BM = 128;       // rows of a CTA's tile (a pair covers 2 * BM)
 constexpr int BN = 256;
 constexpr int BK = 64;        // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;    // K per kind::f16 instruction
-constexpr int STAGES = 4;
 constexpr int CHUNK_KB = 16;  // k-blocks per exact fp32 chunk (16 * 64 = 1024 products)
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 32 * (2 + EPI_WARPS);
 constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int OUT_COLS = 32;                                // columns per TMA store box
-constexpr uint32_t OUT_BUF_BYTES = 32 * OUT_COLS * 2;       // 32 rows x 64 bytes
+constexpr int B_BOX_ROWS = BN / 2;                       // weight rows per TMA box
+constexpr uint32_t B_BOX_BYTES = B_BOX_ROWS * BK * 2;
+constexpr int OUT_COLS = 32;                             // columns per TMA store box
+constexpr uint32_t OUT_BUF_BYTES = 32 * OUT_COLS * 2;    // 32 rows x 64 bytes
 constexpr uint32_t OUT_BYTES = EPI_WARPS * 2 * OUT_BUF_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t BAR_BYTES = 256;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
-constexpr uint32_t IDESC = idesc_bf16_f32<BM, BN>();
-constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s per wait
+constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull;   // 2 s per wait
 
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+// Per-mode shapes: a pair CTA stages 128 weight rows per k-block, a single CTA 256.
+template <bool PAIR>
+struct Mode {
+    static constexpr uint32_t B_BYTES = PAIR ? B_BOX_BYTES : 2 * B_BOX_BYTES;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr uint32_t TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;  // counted on one barrier
+    static constexpr uint32_t IDESC = PAIR ? idesc_bf16_f32<2 * BM, BN>() : idesc_bf16_f32<BM, BN>();
+    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+};
 
 struct Args {
     int64_t M, N, K;
@@ -75,21 +93,22 @@ struct Args {
     const float* ws;
     const __nv_bfloat16* bias;
     int32_t* acc;
-    int64_t num_tiles;
-    int tiles_m, tiles_n, num_kb, group_m;
+    int64_t num_units;      // pair-tiles (pairs) or tiles
+    int unit_rows;          // tile rows per unit: 2 (pairs) or 1
+    int units_m, tiles_m, tiles_n, num_kb, group_m;
     int scalar_scales;
     uint64_t timeout_ns;
 };
 
-// Tile t -> (tile row, tile column) in grouped order.
-__device__ __forceinline__ void tile_coords(int64_t t, const Args& a, int& mb, int& nb)
+// Unit u (a pair-tile, or a tile) -> (unit row, tile column) in grouped order.
+__device__ __forceinline__ void unit_coords(int64_t u, const Args& a, int& um, int& nb)
 {
     const int64_t per_group = (int64_t)a.group_m * a.tiles_n;
-    const int64_t g = t / per_group;
+    const int64_t g = u / per_group;
     const int64_t first = g * a.group_m;
-    const int64_t rows = min((int64_t)a.group_m, (int64_t)a.tiles_m - first);
-    const int64_t r = t - g * per_group;
-    mb = (int)(first + r % rows);
+    const int64_t rows = min((int64_t)a.group_m, (int64_t)a.units_m - first);
+    const int64_t r = u - g * per_group;
+    um = (int)(first + r % rows);
     nb = (int)(r / rows);
 }
 
@@ -116,15 +135,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <bool RAW>
+// 10 warps put three warps on two of the four SM sub-partitions, whose register files
+// hold 16K registers each: at most 168 registers per thread.
+template <bool RAW, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const Args args)
 {
+    using MD = Mode<PAIR>;
+    constexpr int STAGES = MD::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* s_ab = smem;
-    uint8_t* s_out = smem + (size_t)STAGES * STAGE_BYTES;
+    uint8_t* s_out = smem + (size_t)STAGES * MD::STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_out + OUT_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
@@ -137,6 +160,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     unsigned int* err = &g_device_error;
+    const int rank = PAIR ? (int)cluster_ctarank() : 0;  // 0 = leader: issues the MMAs
+    const bool leader = rank == 0;
+    const int cluster = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int clusters = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    constexpr uint16_t kPairMask = 0x3;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -145,7 +173,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], EPI_WARPS);
+            mbar_init(&acc_empty[b], PAIR ? 2 * EPI_WARPS : EPI_WARPS);  // pair: both CTAs' epilogues
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -157,11 +185,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_prefetch_desc(&tmY);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
+    __syncwarp();  // reconverge warps 0 and 1 after their one-lane / one-warp set-up
     tc_fence_before();
-    __syncthreads();
+    if (PAIR)
+        cluster_sync();  // both CTAs' barriers and TMEM exist before either is used
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // everything above overlapped the previous kernel; from here on global memory is read
@@ -175,19 +212,30 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t issued_mask = 0;       // stages holding a load
             uint32_t issued_parity = 0;     // parity of that load's phase, per stage
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
-                int mb, nb;
-                tile_coords(t, args, mb, nb);
-                const int32_t m0 = mb * BM, n0 = nb * BN;
+            for (int64_t u = cluster; ok && u < args.num_units; u += clusters) {
+                int um, nb;
+                unit_coords(u, args, um, nb);
+                const int32_t m0 = (um * args.unit_rows + rank) * BM, n0 = nb * BN;
                 for (int kb = 0; kb < args.num_kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kErrWaitProducer, args.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* sa = s_ab + (size_t)stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
-                    tma_load_2d(sa + A_BYTES, &tmB, &full[stage], kb * BK, n0);
+                    uint8_t* sa = s_ab + (size_t)stage * MD::STAGE_BYTES;
+                    uint8_t* sb = sa + A_BYTES;
+                    if (PAIR) {
+                        // both CTAs' bytes are counted on the leader's barrier
+                        const uint32_t bar = mapa_shared(&full[stage], 0);
+                        if (leader)
+                            mbar_arrive_expect_tx(&full[stage], MD::TX_BYTES);
+                        tma_load_2d_pair(sa, &tmA, bar, kb * BK, m0);
+                        tma_load_2d_pair(sb, &tmB, bar, kb * BK, n0 + rank * B_BOX_ROWS);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], MD::TX_BYTES);
+                        tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
+                        tma_load_2d(sb, &tmB, &full[stage], kb * BK, n0);
+                        tma_load_2d(sb + B_BOX_BYTES, &tmB, &full[stage], kb * BK, n0 + B_BOX_ROWS);
+                    }
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -196,21 +244,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            if (!ok) {
-                // the CTA is aborting: let every issued copy land before shared memory is released
+            if (!ok && leader) {
+                // the CTA is aborting: let every issued copy land before shared memory is
+                // released (the leader's barriers count both CTAs' bytes)
                 for (int s = 0; s < STAGES; ++s)
                     if (issued_mask & (1u << s))
                         drain_wait(&full[s], (issued_parity >> s) & 1u, err, args.timeout_ns);
             }
         }
+        __syncwarp();  // reconverge before the block-wide barrier below
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t acc_iter = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+            for (int64_t u = cluster; ok && u < args.num_units; u += clusters) {
                 for (int kb0 = 0; kb0 < args.num_kb; kb0 += CHUNK_KB) {
                     const uint32_t buf = acc_iter & 1u;
                     const uint32_t acc_phase = (acc_iter >> 1) & 1u;
@@ -227,15 +277,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a0 = smem_u32(s_ab + (size_t)stage * STAGE_BYTES);
+                        const uint32_t a0 = smem_u32(s_ab + (size_t)stage * MD::STAGE_BYTES);
                         const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k) {
                             // +32 bytes per 16-element K step inside the 128-byte swizzle row
-                            mma_bf16(d_tmem, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), IDESC,
-                                     (kb > kb0 || k > 0) ? 1u : 0u);
+                            const uint64_t ad = desc_kmajor_sw128(a0 + k * 32), bd = desc_kmajor_sw128(b0 + k * 32);
+                            const uint32_t accumulate = (kb > kb0 || k > 0) ? 1u : 0u;
+                            if (PAIR)
+                                mma_bf16_pair(d_tmem, ad, bd, MD::IDESC, accumulate);
+                            else
+                                mma_bf16(d_tmem, ad, bd, MD::IDESC, accumulate);
                         }
-                        mma_commit(&empty[stage]);
+                        if (PAIR)
+                            mma_commit_pair(&empty[stage], kPairMask);  // frees the stage in both CTAs
+                        else
+                            mma_commit(&empty[stage]);
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -243,14 +300,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     if (!ok)
                         break;
-                    mma_commit(&acc_full[buf]);
+                    if (PAIR)
+                        mma_commit_pair(&acc_full[buf], kPairMask);
+                    else
+                        mma_commit(&acc_full[buf]);
                     ++acc_iter;
                 }
             }
             // every MMA issued above must be complete before TMEM is released
-            mma_commit(drain);
+            if (PAIR)
+                mma_commit_pair(drain, 0x1);
+            else
+                mma_commit(drain);
             drain_wait(drain, 0, err, args.timeout_ns);
         }
+        __syncwarp();  // reconverge before the block-wide barrier below
     } else {
         // ------------------------------------------------------------ epilogue
         const int e = warp - 2;
@@ -261,10 +325,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t acc_iter = 0;
         uint32_t nstore = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
-            int mb, nb;
-            tile_coords(t, args, mb, nb);
-            const int64_t m0 = (int64_t)mb * BM;
+        for (int64_t u = cluster; ok && u < args.num_units; u += clusters) {
+            int um, nb;
+            unit_coords(u, args, um, nb);
+            const int64_t m0 = (int64_t)(um * args.unit_rows + rank) * BM;
             const int64_t n0 = (int64_t)nb * BN;
             int32_t run[128];
 #pragma unroll
@@ -286,18 +350,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + lane_base + buf * BN + half * 128;
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr + g * 32, v);
+                for (int g = 0; g < 8; ++g) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(taddr + g * 16, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        run[g * 32 + j] += __float2int_rz(__uint_as_float(v[j]));  // exact integer
+                    for (int j = 0; j < 16; ++j)
+                        run[g * 16 + j] += __float2int_rz(__uint_as_float(v[j]));  // exact integer
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&acc_empty[buf]);
+                if (lane == 0) {
+                    if (PAIR)
+                        mbar_arrive_cluster(mapa_shared(&acc_empty[buf], 0));  // the leader's MMA waits on it
+                    else
+                        mbar_arrive(&acc_empty[buf]);
+                }
                 ++acc_iter;
             }
             if (!ok)
@@ -395,10 +463,18 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     griddep_launch_dependents();
     tc_fence_before();
-    __syncthreads();
+    // every warp is converged here: all TMEM reads of this CTA are done and, in a pair,
+    // the leader's MMAs (which write this CTA's TMEM and read its shared memory) as well
+    if (PAIR)
+        cluster_sync();
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -462,7 +538,7 @@ static bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ba
     return true;
 }
 
-template <bool RAW>
+template <bool RAW, bool PAIR>
 static cudaError_t ensure_smem_attr(int device)
 {
     static bool done[64] = {};
@@ -470,11 +546,56 @@ static cudaError_t ensure_smem_attr(int device)
     std::lock_guard<std::mutex> lock(mu);
     if (device >= 0 && device < 64 && done[device])
         return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemm::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)gemm::Mode<PAIR>::SMEM_BYTES);
     if (e == cudaSuccess && device >= 0 && device < 64)
         done[device] = true;
     return e;
+}
+
+// Launch with programmatic stream serialization and, for pairs, 2-CTA clusters.  The
+// persistent grid is as many CTAs (pairs) as can be resident at once: a pair needs two
+// SMs of one GPC, so the count comes from the occupancy calculator, not the SM count.
+template <bool RAW, bool PAIR>
+static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
+                                 const gemm::Args& a, const DeviceInfo& dev, cudaStream_t s)
+{
+    using namespace gemm;
+    cudaError_t e = ensure_smem_attr<RAW, PAIR>(dev.device);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = Mode<PAIR>::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = PAIR ? 2 : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 2 : 1;
+    int64_t resident = dev.sm_count;
+    if (PAIR) {
+        static int cached[64] = {};
+        static std::mutex mu;
+        std::lock_guard<std::mutex> lock(mu);
+        int& n = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
+        if (n == 0) {
+            cfg.gridDim = dim3(2 * (dev.sm_count / 2));
+            e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<RAW, PAIR>, &cfg);
+            if (e != cudaSuccess)
+                return e;
+            if (n <= 0)
+                return cudaErrorInvalidConfiguration;
+        }
+        resident = n;  // clusters
+    }
+    const int64_t units = std::min<int64_t>(a.num_units, resident);
+    cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units));
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR>, tmA, tmB, tmY, a);
 }
 
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why)
@@ -484,7 +605,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     CUtensorMap tmA, tmB, tmY;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, p.K, p.M, (uint64_t)p.K * 2, BK, BM,
                      CU_TENSOR_MAP_SWIZZLE_128B, why) ||
-        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.b, p.K, p.N, (uint64_t)p.K * 2, BK, BN,
+        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.b, p.K, p.N, (uint64_t)p.K * 2, BK, B_BOX_ROWS,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
         return cudaErrorInvalidValue;
     if (raw) {
@@ -503,18 +624,21 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.acc = p.acc;
     a.tiles_m = (int)((p.M + BM - 1) / BM);
     a.tiles_n = (int)((p.N + BN - 1) / BN);
-    a.num_tiles = (int64_t)a.tiles_m * a.tiles_n;
     a.num_kb = (int)((p.K + BK - 1) / BK);
-    a.group_m = 8;
     a.scalar_scales = p.scalar_scales;
     a.timeout_ns = DEFAULT_TIMEOUT_NS;
-    const int grid = (int)std::min<int64_t>(a.num_tiles, dev.sm_count);
-    cudaError_t e = raw ? ensure_smem_attr<true>(dev.device) : ensure_smem_attr<false>(dev.device);
-    if (e != cudaSuccess)
-        return e;
+    // CK_GEMM_PAIR=0 forces one CTA per 128 x 256 tile (A/B timing of the same work)
+    const char* force = std::getenv("CK_GEMM_PAIR");
+    const bool pair = a.tiles_m >= 2 && !(force && std::strcmp(force, "0") == 0);
+    a.unit_rows = pair ? 2 : 1;
+    a.units_m = (a.tiles_m + a.unit_rows - 1) / a.unit_rows;
+    a.num_units = (int64_t)a.units_m * a.tiles_n;
+    a.group_m = pair ? 4 : 8;  // 8 tile rows per sweep either way
     if (raw)
-        return launch_pdl(gemm_kernel<true>, grid, THREADS, SMEM_BYTES, s, tmA, tmB, tmY, a);
-    return launch_pdl(gemm_kernel<false>, grid, THREADS, SMEM_BYTES, s, tmA, tmB, tmY, a);
+        return pair ? launch_kernel<true, true>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<true, false>(tmA, tmB, tmY, a, dev, s);
+    return pair ? launch_kernel<false, true>(tmA, tmB, tmY, a, dev, s)
+                : launch_kernel<false, false>(tmA, tmB, tmY, a, dev, s);
 }
 
 cudaError_t read_device_error(unsigned int* value, bool clear)

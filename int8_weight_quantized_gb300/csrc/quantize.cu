@@ -86,22 +86,29 @@ struct Quantizer {
             kind = 2;
         }
     }
-    __device__ __forceinline__ float operator()(float v) const
-    {
-        float t;
-        if (kind == 1) {
-            t = __fmul_rn(v, r);
-            const float e = __fmaf_rn(-t, s, v);
-            t = __fmaf_rn(e, r, t);
-        } else if (kind == 2) {
-            t = __fdiv_rn(v, s);
-        } else {
-            return 0.0f;
-        }
-        t = rintf(t);  // round half to even
-        return fminf(fmaxf(t, -127.0f), 127.0f);
-    }
 };
+
+// Eight values at once, the method chosen once for all eight (the choice is uniform per row).
+__device__ __forceinline__ void quantize8(const Quantizer& qz, const float (&f)[8], float (&qv)[8])
+{
+    if (qz.kind == 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float t = __fmul_rn(f[i], qz.r);
+            const float e = __fmaf_rn(-t, qz.s, f[i]);
+            t = __fmaf_rn(e, qz.r, t);
+            qv[i] = fminf(fmaxf(rintf(t), -127.0f), 127.0f);
+        }
+    } else if (qz.kind == 2) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            qv[i] = fminf(fmaxf(rintf(__fdiv_rn(f[i], qz.s)), -127.0f), 127.0f);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            qv[i] = 0.0f;
+    }
+}
 
 template <bool OUT8, bool OUT16>
 __device__ __forceinline__ void store8(const float (&qv)[8], int8_t* q8, __nv_bfloat16* q16, int64_t off)
@@ -158,93 +165,82 @@ __device__ __forceinline__ void fwht_slot(float (&v)[8], int lane)
         v[e] = __fmul_rn(v[e], c128);
 }
 
-// Per-row quantize with the row held in registers (K <= 256 * VPT).
-template <int VPT, bool OUT8, bool OUT16>
-__global__ void __launch_bounds__(THREADS) rows_plain_kernel(const uint4* __restrict__ x, int64_t M, int64_t K,
-                                                             int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
-                                                             float* __restrict__ xs)
+// Per-row quantize with the row held in registers: TPR threads per row (one to eight
+// warps), VPT 16-byte vectors per thread, K <= 8 * TPR * VPT.  Vector j of thread t is
+// row vector t + TPR*j, so a warp's 32 lanes hold 32 consecutive vectors (two ConvRot
+// blocks) in every slot.  The row maximum is reduced by shuffles, then across the
+// row's warps through shared memory.
+template <int TPR, int VPT, bool ROT, bool OUT8, bool OUT16>
+__global__ void __launch_bounds__(THREADS) rows_kernel(const uint4* __restrict__ x, int64_t M, int64_t K,
+                                                       int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
+                                                       float* __restrict__ xs)
 {
     griddep_wait();
     griddep_launch_dependents();
+    constexpr int RPB = THREADS / TPR;  // rows per block
+    constexpr int WPR = TPR / 32;       // warps per row
+    __shared__ float red[THREADS / 32];
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
-    if (row >= M)
-        return;
+    const int t = threadIdx.x % TPR;
+    const int g = threadIdx.x / TPR;
+    const int64_t row = (int64_t)blockIdx.x * RPB + g;
+    const bool live = row < M;
     const int64_t nvec = K >> 3;
-    const uint4* xr = x + row * nvec;
+    const uint4* xr = x + (live ? row : 0) * nvec;
+    const int64_t warp_first = t - lane;  // first vector of this warp in slot 0
+
+    float v[VPT][8];
     uint4 raw[VPT];
+    float amax = 0.0f;
     __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-        const int64_t idx = lane + 32 * j;
-        raw[j] = (idx < nvec) ? ld_stream(xr + idx) : make_uint4(0, 0, 0, 0);
-        m2 = absmax8(m2, raw[j]);
+        const int64_t idx = t + (int64_t)TPR * j;
+        raw[j] = (live && idx < nvec) ? ld_stream(xr + idx) : make_uint4(0, 0, 0, 0);
+        if (!ROT)
+            m2 = absmax8(m2, raw[j]);
     }
-    const float amax = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
-    const float s = __fdiv_rn(amax, 127.0f);
-    if (lane == 0)
-        xs[row] = s;
-    const Quantizer qz(s, false);
+    if (ROT) {
 #pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        const int64_t idx = lane + 32 * j;
-        if (idx < nvec) {
-            float f[8], qv[8];
-            unpack8(raw[j], f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                qv[i] = qz(f[i]);
-            store8<OUT8, OUT16>(qv, q8, q16, row * K + idx * 8);
-        }
-    }
-}
-
-// ConvRot per-row quantize with the rotated row held in registers (K <= 256 * VPT).
-template <int VPT, bool OUT8, bool OUT16>
-__global__ void __launch_bounds__(THREADS) rows_rot_kernel(const uint4* __restrict__ x, int64_t M, int64_t K,
-                                                           int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
-                                                           float* __restrict__ xs)
-{
-    griddep_wait();
-    griddep_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
-    if (row >= M)
-        return;
-    const int64_t nvec = K >> 3;
-    const uint4* xr = x + row * nvec;
-    float v[VPT][8];
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        const int64_t idx = lane + 32 * j;
-        const uint4 r = (idx < nvec) ? ld_stream(xr + idx) : make_uint4(0, 0, 0, 0);
-        unpack8(r, v[j]);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        if (32 * j < nvec) {  // warp-uniform: slot j holds at least one block
-            fwht_slot(v[j], lane);
-            if (lane + 32 * j < nvec) {
+        for (int j = 0; j < VPT; ++j) {
+            unpack8(raw[j], v[j]);
+            if (warp_first + (int64_t)TPR * j < nvec) {  // warp-uniform
+                fwht_slot(v[j], lane);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     amax = fmaxf(amax, fabsf(v[j][e]));
             }
         }
+    } else {
+        amax = fmaxf(__low2float(m2), __high2float(m2));
     }
     amax = warp_max(amax);
+    if (WPR > 1) {
+        if (lane == 0)
+            red[threadIdx.x >> 5] = amax;
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < WPR; ++i)
+            amax = fmaxf(amax, red[g * WPR + i]);
+    }
+    if (!live)
+        return;
     const float s = __fdiv_rn(amax, 127.0f);
-    if (lane == 0)
+    if (t == 0)
         xs[row] = s;
-    const Quantizer qz(s, true);
+    const Quantizer qz(s, ROT);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-        const int64_t idx = lane + 32 * j;
+        const int64_t idx = t + (int64_t)TPR * j;
         if (idx < nvec) {
             float qv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                qv[i] = qz(v[j][i]);
+            if (ROT) {
+                quantize8(qz, v[j], qv);
+            } else {
+                float f[8];
+                unpack8(raw[j], f);
+                quantize8(qz, f, qv);
+            }
             store8<OUT8, OUT16>(qv, q8, q16, row * K + idx * 8);
         }
     }
@@ -292,9 +288,7 @@ __global__ void __launch_bounds__(THREADS) rows_stream_kernel(const uint4* __res
         if (ROT)
             fwht_slot(f, lane);
         if (idx < nvec) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                qv[i] = qz(f[i]);
+            quantize8(qz, f, qv);
             store8<OUT8, OUT16>(qv, q8, q16, row * K + idx * 8);
         }
     }
@@ -376,9 +370,7 @@ __global__ void __launch_bounds__(256) quant_flat_kernel(const uint4* __restrict
             if (i < nvec) {
                 float f[8], qv[8];
                 unpack8(v[u], f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    qv[e] = qz(f[e]);
+                quantize8(qz, f, qv);
                 store8<OUT8, OUT16>(qv, q8, q16, i * 8);
             }
         }
@@ -441,33 +433,42 @@ cudaError_t rows_dispatch(const void* x, int64_t M, int64_t K, bool rotate, int8
     using namespace quant;
     const uint4* xv = static_cast<const uint4*>(x);
     __nv_bfloat16* q16b = static_cast<__nv_bfloat16*>(q16);
-    const int64_t blocks64 = (M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
-    if (blocks64 > 0x7FFFFFFF)
+    const int64_t nvec = K / 8;
+    // threads per row: the fewest (32..256) that keep at most 4 vectors per thread,
+    // 8 vectors for the longest register-resident rows (K <= 16384)
+    int tpr, vpt;
+    if (nvec <= 128) { tpr = 32; vpt = 4; }
+    else if (nvec <= 256) { tpr = 64; vpt = 4; }
+    else if (nvec <= 512) { tpr = 128; vpt = 4; }
+    else if (nvec <= 1024) { tpr = 256; vpt = 4; }
+    else if (nvec <= 2048) { tpr = 256; vpt = 8; }
+    else { tpr = 0; vpt = 0; }
+    if (tpr == 0) {
+        const int64_t blocks = (M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
+        if (blocks > 0x7FFFFFFF)
+            return cudaErrorInvalidValue;
+        if (rotate)
+            return launch_pdl(rows_stream_kernel<true, OUT8, OUT16>, (unsigned)blocks, THREADS, 0, s, xv, M, K, q8,
+                              q16b, xs);
+        return launch_pdl(rows_stream_kernel<false, OUT8, OUT16>, (unsigned)blocks, THREADS, 0, s, xv, M, K, q8,
+                          q16b, xs);
+    }
+    const int64_t rpb = THREADS / tpr;
+    const int64_t blocks = (M + rpb - 1) / rpb;
+    if (blocks > 0x7FFFFFFF)
         return cudaErrorInvalidValue;
-    const unsigned grid = (unsigned)blocks64;
-    const int64_t slots = (K + 255) / 256;  // 16-byte vectors per lane
-    cudaError_t e = cudaSuccess;
-#define CK_ROWS(KERNEL, V) e = launch_pdl(KERNEL<V, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs)
-    if (!rotate) {
-        if (slots <= 1) CK_ROWS(rows_plain_kernel, 1);
-        else if (slots <= 2) CK_ROWS(rows_plain_kernel, 2);
-        else if (slots <= 4) CK_ROWS(rows_plain_kernel, 4);
-        else if (slots <= 8) CK_ROWS(rows_plain_kernel, 8);
-        else if (slots <= 12) CK_ROWS(rows_plain_kernel, 12);
-        else if (slots <= 16) CK_ROWS(rows_plain_kernel, 16);
-        else if (slots <= 24) CK_ROWS(rows_plain_kernel, 24);
-        else e = launch_pdl(rows_stream_kernel<false, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs);
-    } else {
-        if (slots <= 1) CK_ROWS(rows_rot_kernel, 1);
-        else if (slots <= 2) CK_ROWS(rows_rot_kernel, 2);
-        else if (slots <= 4) CK_ROWS(rows_rot_kernel, 4);
-        else if (slots <= 8) CK_ROWS(rows_rot_kernel, 8);
-        else if (slots <= 12) CK_ROWS(rows_rot_kernel, 12);
-        else if (slots <= 16) CK_ROWS(rows_rot_kernel, 16);
-        else e = launch_pdl(rows_stream_kernel<true, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs);
+    const unsigned grid = (unsigned)blocks;
+#define CK_ROWS(T, V)                                                                                   \
+    (rotate ? launch_pdl(rows_kernel<T, V, true, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs) \
+            : launch_pdl(rows_kernel<T, V, false, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs))
+    switch (tpr * 16 + vpt) {
+    case 32 * 16 + 4: return CK_ROWS(32, 4);
+    case 64 * 16 + 4: return CK_ROWS(64, 4);
+    case 128 * 16 + 4: return CK_ROWS(128, 4);
+    case 256 * 16 + 4: return CK_ROWS(256, 4);
+    default: return CK_ROWS(256, 8);
     }
 #undef CK_ROWS
-    return e;
 }
 
 }  // namespace
@@ -478,8 +479,6 @@ cudaError_t launch_quantize_rows(const void* x, int64_t M, int64_t K, bool rotat
     (void)dev;
     if (M == 0)
         return cudaSuccess;
-    if (q8 && q16)
-        return rows_dispatch<true, true>(x, M, K, rotate, q8, q16, x_scale, s);
     if (q8)
         return rows_dispatch<true, false>(x, M, K, rotate, q8, q16, x_scale, s);
     return rows_dispatch<false, true>(x, M, K, rotate, q8, q16, x_scale, s);

@@ -20,9 +20,12 @@ def gpu_acc(q, w):
     return acc.cpu().numpy()
 
 
-# several tiles, ragged M/N/K tails, one and several 1024-wide K chunks
+# several tiles, ragged M/N/K tails, one and several 1024-wide K chunks; single tile rows
+# (unpaired CTAs) and odd numbers of tile rows (the last CTA pair's second tile lies
+# wholly below M)
 @pytest.mark.parametrize("M,N,K", [(256, 512, 512), (1, 8, 16), (129, 264, 80), (300, 520, 1040),
-                                   (128, 256, 2048), (1000, 776, 3088), (77, 1032, 5376)])
+                                   (128, 256, 2048), (1000, 776, 3088), (77, 1032, 5376), (384, 256, 256),
+                                   (640, 1280, 1024), (2304, 512, 160)])
 def test_s32_parity(M, N, K):
     q = synthetic.int8_uniform((M, K), seed=M + K)
     w = synthetic.int8_uniform((N, K), seed=N + 7 * K)
@@ -65,7 +68,7 @@ def test_s32_int32_range_end():
 
 @pytest.mark.parametrize("scalar", [False, True])
 @pytest.mark.parametrize("with_bias", [False, True])
-@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (129, 264, 1040), (1, 8, 16)])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (129, 264, 1040), (1, 8, 16), (385, 520, 192)])
 def test_dequant_parity(M, N, K, scalar, with_bias):
     q = synthetic.int8_uniform((M, K), seed=11 + M)
     w = synthetic.int8_uniform((N, K), seed=12 + N)

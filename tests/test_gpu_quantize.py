@@ -25,15 +25,16 @@ def check_rowwise(x_cpu, rotate):
         len(bad), bad[0], qn[tuple(bad[0])], q_ref[tuple(bad[0])])
 
 
-# register-resident paths (K <= 6144), ragged tails of the 256-element lane slots, and
-# the two-pass path for long rows (K > 6144)
+# register-resident paths for every threads-per-row choice (32..256 threads, 4 or 8
+# vectors each: K up to 16384), ragged row tails, and the two-pass path for longer rows
 @pytest.mark.parametrize("M,K", [(256, 512), (37, 16), (9, 48), (100, 2048), (3, 6144), (5, 5376),
-                                 (7, 6160), (2, 65536)])
+                                 (7, 6160), (13, 4096), (3, 12288), (2, 16384), (2, 16400), (2, 65536)])
 def test_rowwise_parity(M, K):
     check_rowwise(synthetic.normal_bf16((M, K), seed=100 + K), rotate=False)
 
 
-@pytest.mark.parametrize("M,K", [(64, 128), (33, 384), (16, 4096), (3, 8192), (2, 4224)])
+@pytest.mark.parametrize("M,K", [(64, 128), (33, 384), (16, 4096), (3, 8192), (2, 4224), (3, 12288),
+                                 (2, 16384), (2, 16512)])
 def test_rowwise_convrot_parity(M, K):
     oc = synthetic.outlier_columns(K, 0.01, seed=7)
     check_rowwise(synthetic.normal_bf16((M, K), seed=200 + K, outlier_channels=oc), rotate=True)
