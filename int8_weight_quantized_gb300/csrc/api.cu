@@ -90,20 +90,20 @@ int check_device(DeviceInfo* dev)
             return fail(CK_ERR_INVALID_ARG, "%s must be 16-byte aligned", #p);                  \
     } while (0)
 
-constexpr int kMaxPartialsForLayout = 1024;  // tensorwise partial maxima region (floats)
+constexpr int kMaxPartialsForLayout = 1024;  // most blocks that exchange tensorwise maxima
 
 struct LinearWorkspace {
     void* a16;        // bf16 [M,K]: quantized activation as tensor-core operand
     void* b16;        // bf16 [N,K]: weight as tensor-core operand
     float* xs;        // fp32 [M] or [1]
-    float* partials;  // tensorwise partial maxima
+    void* scratch;    // tensorwise: the blocks' maxima, exchanged within one launch
 };
 
 size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int mode, int nparts)
 {
     return align_up((size_t)M * K * 2) + align_up((size_t)N * K * 2) +
            align_up(sizeof(float) * (size_t)(mode == CK_TENSORWISE ? 1 : (M > 0 ? M : 1))) +
-           align_up(sizeof(float) * (size_t)nparts);
+           align_up(prep_tensorwise_scratch_bytes(nparts));
 }
 
 LinearWorkspace carve_linear(void* ws, int64_t M, int64_t N, int64_t K, int mode)
@@ -116,7 +116,7 @@ LinearWorkspace carve_linear(void* ws, int64_t M, int64_t N, int64_t K, int mode
     p += align_up((size_t)N * K * 2);
     w.xs = reinterpret_cast<float*>(p);
     p += align_up(sizeof(float) * (size_t)(mode == CK_TENSORWISE ? 1 : (M > 0 ? M : 1)));
-    w.partials = reinterpret_cast<float*>(p);
+    w.scratch = p;
     return w;
 }
 
@@ -330,25 +330,21 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
         return st;
     if (M == 0)
         return CK_OK;
-    log_shape("int8_linear", M, N, K, mode, "tcgen05-bf16-exact 128x256x64 s4");
+    log_shape("int8_linear", M, N, K, mode, "prep(1 launch) + tcgen05 bf16-exact GEMM, 2-CTA 256x256 tiles");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     LinearWorkspace ws = carve_linear(workspace, M, N, K, mode);
     cudaError_t e;
     {
-        ProfScope ps(kProfQuantize, mode == CK_TENSORWISE ? 2 : 1, s);
+        // one launch: quantize the activation into bf16 codes and widen the weight
+        ProfScope ps(kProfQuantize, 1, s);
         if (mode == CK_TENSORWISE)
-            e = launch_quantize_tensorwise(x, M, K, nullptr, ws.a16, ws.xs, ws.partials, dev, s);
+            e = launch_prep_tensorwise(x, M, K, ws.a16, ws.xs, ws.scratch, kMaxPartialsForLayout, w, N * K, ws.b16,
+                                       dev, s);
         else
-            e = launch_quantize_rows(x, M, K, mode == CK_CONVROT, nullptr, ws.a16, ws.xs, dev, s);
+            e = launch_prep_rows(x, M, K, mode == CK_CONVROT, ws.a16, ws.xs, w, N * K, ws.b16, dev, s);
     }
     if (e != cudaSuccess)
-        return cuda_fail(e, "ck_int8_linear quantize launch");
-    {
-        ProfScope ps(kProfWiden, 1, s);
-        e = launch_widen_int8(w, ws.b16, N * K, dev, s);
-    }
-    if (e != cudaSuccess)
-        return cuda_fail(e, "ck_int8_linear weight widening launch");
+        return cuda_fail(e, "ck_int8_linear preparation launch");
     GemmProblem p;
     p.a = ws.a16;
     p.b = ws.b16;
@@ -406,16 +402,15 @@ static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, co
         return st;
     if (M == 0)
         return CK_OK;
-    log_shape(name, M, N, K, scalar_scales ? CK_TENSORWISE : CK_PER_ROW, "tcgen05-bf16-exact 128x256x64 s4");
+    log_shape(name, M, N, K, scalar_scales ? CK_TENSORWISE : CK_PER_ROW, "widen(1 launch) + tcgen05 bf16-exact GEMM, 2-CTA 256x256 tiles");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* p8 = static_cast<uint8_t*>(workspace);
     void* a16 = p8;
     void* b16 = p8 + align_up((size_t)M * K * 2);
     cudaError_t e;
     {
-        ProfScope ps(kProfWiden, 2, s);
-        if ((e = launch_widen_int8(q, a16, M * K, dev, s)) == cudaSuccess)
-            e = launch_widen_int8(w, b16, N * K, dev, s);
+        ProfScope ps(kProfWiden, 1, s);
+        e = launch_widen2(q, M * K, a16, w, N * K, b16, dev, s);
     }
     if (e != cudaSuccess)
         return cuda_fail(e, "operand widening launch");

@@ -16,6 +16,7 @@ enum : uint32_t {
     kErrWaitEpilogue = 1u << 2,  // epilogue gave up waiting for an accumulator
     kErrWaitDrain = 1u << 3,     // teardown gave up waiting for in-flight copies / MMAs
     kErrWaitSelfTest = 1u << 4,  // the wait self-test timed out (expected by that test)
+    kErrWaitGrid = 1u << 5,      // a grid-wide barrier of a preparation kernel timed out
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)

@@ -71,6 +71,22 @@ cudaError_t launch_quantize_tensorwise(const void* x, int64_t M, int64_t K, int8
 cudaError_t launch_quantize_tensorwise_parts(const void* x, int64_t M, int64_t K, int8_t* q8, void* q16,
                                              float* x_scale, float* partials, int nparts, const DeviceInfo& dev,
                                              cudaStream_t s);
+// The layer's preparation in one launch: quantize the activation into bf16 codes (and
+// its scales) and widen the int8 weight w8 (w_n values) into w16.  Per-row / ConvRot:
+// the row kernel takes a share of the widening.  Tensorwise: a single kernel whose
+// blocks exchange their maxima through `scratch` (prep_tensorwise_scratch_bytes(max_blocks)
+// bytes of workspace; its content on entry does not matter).
+cudaError_t launch_prep_rows(const void* x, int64_t M, int64_t K, bool rotate, void* q16, float* x_scale,
+                             const int8_t* w8, int64_t w_n, void* w16, const DeviceInfo& dev, cudaStream_t s);
+size_t prep_tensorwise_scratch_bytes(int max_blocks);
+cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q16, float* x_scale, void* scratch,
+                                   int max_blocks, const int8_t* w8, int64_t w_n, void* w16, const DeviceInfo& dev,
+                                   cudaStream_t s);
+// Two int8 -> bf16 widenings in one launch.
+cudaError_t launch_widen2(const int8_t* a8, int64_t a_n, void* a16, const int8_t* b8, int64_t b_n, void* b16,
+                          const DeviceInfo& dev, cudaStream_t s);
+// Device address of the library's error word on the current device.
+cudaError_t device_error_ptr(unsigned int** ptr);
 // int8 -> bf16 widening of n values (n % 16 == 0).
 cudaError_t launch_widen_int8(const int8_t* src, void* dst, int64_t n, const DeviceInfo& dev, cudaStream_t s);
 

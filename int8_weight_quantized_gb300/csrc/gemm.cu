@@ -58,14 +58,14 @@ __device__ unsigned int g_device_error;
 namespace gemm {
 
 constexpr int BM = 128;       // rows of a CTA's tile (a pair covers 2 * BM)
-constexpr int BN = 256;
+constexpr int BN = 256;       // widest tile; a launch may use any multiple of 32 up to it
 constexpr int BK = 64;        // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;    // K per kind::f16 instruction
 constexpr int CHUNK_KB = 16;  // k-blocks per exact fp32 chunk (16 * 64 = 1024 products)
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 32 * (2 + EPI_WARPS);
 constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr int B_BOX_ROWS = BN / 2;                       // weight rows per TMA box
+constexpr int B_BOX_ROWS = BN / 2;                       // most weight rows per TMA box
 constexpr uint32_t B_BOX_BYTES = B_BOX_ROWS * BK * 2;
 constexpr int OUT_COLS = 32;                             // columns per TMA store box
 constexpr uint32_t OUT_BUF_BYTES = 32 * OUT_COLS * 2;    // 32 rows x 64 bytes
@@ -80,8 +80,7 @@ struct Mode {
     static constexpr uint32_t B_BYTES = PAIR ? B_BOX_BYTES : 2 * B_BOX_BYTES;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = PAIR ? 6 : 4;
-    static constexpr uint32_t TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;  // counted on one barrier
-    static constexpr uint32_t IDESC = PAIR ? idesc_bf16_f32<2 * BM, BN>() : idesc_bf16_f32<BM, BN>();
+    static constexpr uint32_t IDESC_M = PAIR ? idesc_bf16_f32<2 * BM, 0>() : idesc_bf16_f32<BM, 0>();
     static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
@@ -95,6 +94,9 @@ struct Args {
     int32_t* acc;
     int64_t num_units;      // pair-tiles (pairs) or tiles
     int unit_rows;          // tile rows per unit: 2 (pairs) or 1
+    int bn;                 // tile width in N (multiple of 32, <= BN)
+    uint32_t idesc;         // MMA instruction descriptor for this width
+    uint32_t tx_bytes;      // bytes of one k-block counted on the (leader's) full barrier
     int units_m, tiles_m, tiles_n, num_kb, group_m;
     int scalar_scales;
     uint64_t timeout_ns;
@@ -215,7 +217,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int64_t u = cluster; ok && u < args.num_units; u += clusters) {
                 int um, nb;
                 unit_coords(u, args, um, nb);
-                const int32_t m0 = (um * args.unit_rows + rank) * BM, n0 = nb * BN;
+                const int32_t m0 = (um * args.unit_rows + rank) * BM, n0 = nb * args.bn;
+                const int half_rows = args.bn >> 1;  // weight rows per box
                 for (int kb = 0; kb < args.num_kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kErrWaitProducer, args.timeout_ns)) {
                         ok = false;
@@ -227,14 +230,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // both CTAs' bytes are counted on the leader's barrier
                         const uint32_t bar = mapa_shared(&full[stage], 0);
                         if (leader)
-                            mbar_arrive_expect_tx(&full[stage], MD::TX_BYTES);
+                            mbar_arrive_expect_tx(&full[stage], args.tx_bytes);
                         tma_load_2d_pair(sa, &tmA, bar, kb * BK, m0);
-                        tma_load_2d_pair(sb, &tmB, bar, kb * BK, n0 + rank * B_BOX_ROWS);
+                        tma_load_2d_pair(sb, &tmB, bar, kb * BK, n0 + rank * half_rows);
                     } else {
-                        mbar_arrive_expect_tx(&full[stage], MD::TX_BYTES);
+                        mbar_arrive_expect_tx(&full[stage], args.tx_bytes);
                         tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
                         tma_load_2d(sb, &tmB, &full[stage], kb * BK, n0);
-                        tma_load_2d(sb + B_BOX_BYTES, &tmB, &full[stage], kb * BK, n0 + B_BOX_ROWS);
+                        tma_load_2d(sb + half_rows * BK * 2, &tmB, &full[stage], kb * BK, n0 + half_rows);
                     }
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -285,9 +288,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const uint64_t ad = desc_kmajor_sw128(a0 + k * 32), bd = desc_kmajor_sw128(b0 + k * 32);
                             const uint32_t accumulate = (kb > kb0 || k > 0) ? 1u : 0u;
                             if (PAIR)
-                                mma_bf16_pair(d_tmem, ad, bd, MD::IDESC, accumulate);
+                                mma_bf16_pair(d_tmem, ad, bd, args.idesc, accumulate);
                             else
-                                mma_bf16(d_tmem, ad, bd, MD::IDESC, accumulate);
+                                mma_bf16(d_tmem, ad, bd, args.idesc, accumulate);
                         }
                         if (PAIR)
                             mma_commit_pair(&empty[stage], kPairMask);  // frees the stage in both CTAs
@@ -329,7 +332,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             int um, nb;
             unit_coords(u, args, um, nb);
             const int64_t m0 = (int64_t)(um * args.unit_rows + rank) * BM;
-            const int64_t n0 = (int64_t)nb * BN;
+            const int64_t n0 = (int64_t)nb * args.bn;
+            // columns of the tile in this warp's half: a multiple of 32 in [0, 128]
+            const int ncols = max(0, min(128, args.bn - half * 128));
             int32_t run[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j)
@@ -351,12 +356,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t taddr = tmem_base + lane_base + buf * BN + half * 128;
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(taddr + g * 16, v);
-                    tmem_wait_ld();
+                    if (g * 16 < ncols) {  // warp-uniform
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(taddr + g * 16, v);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        run[g * 16 + j] += __float2int_rz(__uint_as_float(v[j]));  // exact integer
+                        for (int j = 0; j < 16; ++j)
+                            run[g * 16 + j] += __float2int_rz(__uint_as_float(v[j]));  // exact integer
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -379,7 +386,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int c4 = 0; c4 < 32; ++c4) {
                         const int64_t col = cbase + 4 * c4;
-                        if (col < args.N)  // N % 8 == 0: a 4-column group is all in or all out
+                        // N % 8 == 0: a 4-column group is all in or all out
+                        if (4 * c4 < ncols && col < args.N)
                             *reinterpret_cast<int4*>(dst + col) =
                                 make_int4(run[4 * c4], run[4 * c4 + 1], run[4 * c4 + 2], run[4 * c4 + 3]);
                     }
@@ -391,8 +399,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     const int64_t col0 = cbase + g * OUT_COLS;
-                    if (col0 >= args.N || row0 >= args.M)
-                        break;  // warp-uniform: nothing of this box is inside y
+                    if (g * OUT_COLS >= ncols || col0 >= args.N || row0 >= args.M)
+                        break;  // warp-uniform: nothing of this box is inside the tile and y
                     uint8_t* buf = obuf + (nstore & 1u) * OUT_BUF_BYTES;
                     if (lane == 0)
                         bulk_wait_group_read<1>();  // the store that last used `buf` has read it
@@ -553,9 +561,82 @@ static cudaError_t ensure_smem_attr(int device)
     return e;
 }
 
-// Launch with programmatic stream serialization and, for pairs, 2-CTA clusters.  The
-// persistent grid is as many CTAs (pairs) as can be resident at once: a pair needs two
-// SMs of one GPC, so the count comes from the occupancy calculator, not the SM count.
+static cudaLaunchConfig_t make_config(bool pair, size_t smem, cudaStream_t s, cudaLaunchAttribute (&attr)[2])
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(gemm::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = pair ? 2 : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pair ? 2 : 1;
+    return cfg;
+}
+
+// How many units (pairs, or single CTAs) can be resident at once: a pair needs two SMs
+// of one GPC, so for pairs the count comes from the occupancy calculator.
+template <bool PAIR>
+static cudaError_t resident_units(const DeviceInfo& dev, int64_t* out)
+{
+    if (!PAIR) {
+        *out = dev.sm_count;
+        return cudaSuccess;
+    }
+    static int cached[64] = {};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int& n = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
+    if (n == 0) {
+        cudaError_t e = ensure_smem_attr<false, true>(dev.device);
+        if (e == cudaSuccess)
+            e = ensure_smem_attr<true, true>(dev.device);
+        if (e != cudaSuccess)
+            return e;
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = make_config(true, gemm::Mode<true>::SMEM_BYTES, nullptr, attr);
+        cfg.gridDim = dim3(2 * (dev.sm_count / 2));
+        e = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_kernel<false, true>, &cfg);
+        if (e != cudaSuccess)
+            return e;
+        if (n <= 0)
+            return cudaErrorInvalidConfiguration;
+    }
+    *out = n;
+    return cudaSuccess;
+}
+
+// The tile width (a multiple of 32 up to 256) that finishes soonest: `units_m` rows of
+// units times ceil(N / bn) columns run in ceil(units / resident) waves, and a wave costs
+// about bn + 64 column-equivalents (the activation tile costs as much as 64 weight rows
+// to stage).  CK_GEMM_BN=<width> forces a width (A/B timing of the same work).
+static int choose_tile_width(int64_t N, int64_t units_m, int64_t resident)
+{
+    if (const char* force = std::getenv("CK_GEMM_BN")) {
+        const int f = std::atoi(force);
+        if (f >= 32 && f <= gemm::BN && f % 32 == 0)
+            return f;
+    }
+    int best = gemm::BN;
+    int64_t best_cost = -1;
+    for (int bn = gemm::BN; bn >= 128; bn -= 32) {
+        const int64_t units = units_m * ((N + bn - 1) / bn);
+        const int64_t waves = (units + resident - 1) / resident;
+        const int64_t cost = waves * (bn + 64);
+        if (best_cost < 0 || cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+// Launch with programmatic stream serialization and, for pairs, 2-CTA clusters; the
+// persistent grid is as many units as can be resident at once.
 template <bool RAW, bool PAIR>
 static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                                  const gemm::Args& a, const DeviceInfo& dev, cudaStream_t s)
@@ -564,35 +645,11 @@ static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB,
     cudaError_t e = ensure_smem_attr<RAW, PAIR>(dev.device);
     if (e != cudaSuccess)
         return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = Mode<PAIR>::SMEM_BYTES;
-    cfg.stream = s;
+    int64_t resident = 0;
+    if ((e = resident_units<PAIR>(dev, &resident)) != cudaSuccess)
+        return e;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = PAIR ? 2 : 1;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = PAIR ? 2 : 1;
-    int64_t resident = dev.sm_count;
-    if (PAIR) {
-        static int cached[64] = {};
-        static std::mutex mu;
-        std::lock_guard<std::mutex> lock(mu);
-        int& n = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
-        if (n == 0) {
-            cfg.gridDim = dim3(2 * (dev.sm_count / 2));
-            e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<RAW, PAIR>, &cfg);
-            if (e != cudaSuccess)
-                return e;
-            if (n <= 0)
-                return cudaErrorInvalidConfiguration;
-        }
-        resident = n;  // clusters
-    }
+    cudaLaunchConfig_t cfg = make_config(PAIR, Mode<PAIR>::SMEM_BYTES, s, attr);
     const int64_t units = std::min<int64_t>(a.num_units, resident);
     cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units));
     return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR>, tmA, tmB, tmY, a);
@@ -604,8 +661,6 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     const bool raw = p.acc != nullptr;
     CUtensorMap tmA, tmB, tmY;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, p.K, p.M, (uint64_t)p.K * 2, BK, BM,
-                     CU_TENSOR_MAP_SWIZZLE_128B, why) ||
-        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.b, p.K, p.N, (uint64_t)p.K * 2, BK, B_BOX_ROWS,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
         return cudaErrorInvalidValue;
     if (raw) {
@@ -623,17 +678,27 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.bias = reinterpret_cast<const __nv_bfloat16*>(p.bias);
     a.acc = p.acc;
     a.tiles_m = (int)((p.M + BM - 1) / BM);
-    a.tiles_n = (int)((p.N + BN - 1) / BN);
     a.num_kb = (int)((p.K + BK - 1) / BK);
     a.scalar_scales = p.scalar_scales;
     a.timeout_ns = DEFAULT_TIMEOUT_NS;
-    // CK_GEMM_PAIR=0 forces one CTA per 128 x 256 tile (A/B timing of the same work)
+    // CK_GEMM_PAIR=0 forces one CTA per 128-row tile (A/B timing of the same work)
     const char* force = std::getenv("CK_GEMM_PAIR");
     const bool pair = a.tiles_m >= 2 && !(force && std::strcmp(force, "0") == 0);
     a.unit_rows = pair ? 2 : 1;
     a.units_m = (a.tiles_m + a.unit_rows - 1) / a.unit_rows;
-    a.num_units = (int64_t)a.units_m * a.tiles_n;
     a.group_m = pair ? 4 : 8;  // 8 tile rows per sweep either way
+    int64_t resident = 0;
+    const cudaError_t e = pair ? resident_units<true>(dev, &resident) : resident_units<false>(dev, &resident);
+    if (e != cudaSuccess)
+        return e;
+    a.bn = choose_tile_width(p.N, a.units_m, resident);
+    a.tiles_n = (int)((p.N + a.bn - 1) / a.bn);
+    a.num_units = (int64_t)a.units_m * a.tiles_n;
+    a.idesc = (pair ? Mode<true>::IDESC_M : Mode<false>::IDESC_M) | ((uint32_t)(a.bn >> 3) << 17);
+    a.tx_bytes = (pair ? 2u : 1u) * (A_BYTES + (uint32_t)(pair ? a.bn / 2 : a.bn) * BK * 2);
+    if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.b, p.K, p.N, (uint64_t)p.K * 2, BK, a.bn / 2,
+                     CU_TENSOR_MAP_SWIZZLE_128B, why))
+        return cudaErrorInvalidValue;
     if (raw)
         return pair ? launch_kernel<true, true>(tmA, tmB, tmY, a, dev, s)
                     : launch_kernel<true, false>(tmA, tmB, tmY, a, dev, s);
@@ -651,6 +716,28 @@ cudaError_t read_device_error(unsigned int* value, bool clear)
         return e;
     const unsigned int zero = 0;
     return cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+}
+
+cudaError_t device_error_ptr(unsigned int** ptr)
+{
+    static unsigned int* cached[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && cached[dev]) {
+        *ptr = cached[dev];
+        return cudaSuccess;
+    }
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_device_error)) != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64)
+        cached[dev] = static_cast<unsigned int*>(p);
+    *ptr = static_cast<unsigned int*>(p);
+    return cudaSuccess;
 }
 
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s)

@@ -16,7 +16,15 @@
 // pair of bf16 significands (numerator <= maximum) over the full exponent range that
 // can reach rint's decision, with zero mismatches.  Rows with a tiny scale
 // (s < 2^-100) and every ConvRot row (fp32 v) use the IEEE division itself.
+#include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <unistd.h>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -165,15 +173,64 @@ __device__ __forceinline__ void fwht_slot(float (&v)[8], int lane)
         v[e] = __fmul_rn(v[e], c128);
 }
 
+// int8 -> bf16 (exact), 16 values per thread and vector.
+__device__ __forceinline__ void widen16(const uint4& v, uint4& lo, uint4& hi)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float a = (float)(int8_t)((w[k] >> (16 * h)) & 0xFFu);
+            const float b = (float)(int8_t)((w[k] >> (16 * h + 8)) & 0xFFu);
+            __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+            o[2 * k + h] = *reinterpret_cast<uint32_t*>(&p);
+        }
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// This block's share of an int8 -> bf16 widening of n16 16-value vectors, grid-stride
+// over every block of the launch (no-op when src is null).
+__device__ __forceinline__ void widen_share(const uint4* __restrict__ src, int64_t n16, uint4* __restrict__ dst)
+{
+    if (src == nullptr)
+        return;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < n16; base += UNROLL * stride) {
+        uint4 v[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            v[u] = i < n16 ? ld_stream(src + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            if (i < n16) {
+                uint4 lo, hi;
+                widen16(v[u], lo, hi);
+                dst[2 * i] = lo;
+                dst[2 * i + 1] = hi;
+            }
+        }
+    }
+}
+
 // Per-row quantize with the row held in registers: TPR threads per row (one to eight
 // warps), VPT 16-byte vectors per thread, K <= 8 * TPR * VPT.  Vector j of thread t is
 // row vector t + TPR*j, so a warp's 32 lanes hold 32 consecutive vectors (two ConvRot
 // blocks) in every slot.  The row maximum is reduced by shuffles, then across the
 // row's warps through shared memory.
+// With w8 != null the launch also widens the weight (each block takes a share after
+// its rows), so the layer's two bandwidth-bound passes share one launch.
 template <int TPR, int VPT, bool ROT, bool OUT8, bool OUT16>
 __global__ void __launch_bounds__(THREADS) rows_kernel(const uint4* __restrict__ x, int64_t M, int64_t K,
                                                        int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
-                                                       float* __restrict__ xs)
+                                                       float* __restrict__ xs, const uint4* __restrict__ w8,
+                                                       int64_t w_n16, uint4* __restrict__ w16)
 {
     griddep_wait();
     griddep_launch_dependents();
@@ -223,42 +280,37 @@ __global__ void __launch_bounds__(THREADS) rows_kernel(const uint4* __restrict__
         for (int i = 0; i < WPR; ++i)
             amax = fmaxf(amax, red[g * WPR + i]);
     }
-    if (!live)
-        return;
-    const float s = __fdiv_rn(amax, 127.0f);
-    if (t == 0)
-        xs[row] = s;
-    const Quantizer qz(s, ROT);
+    if (live) {
+        const float s = __fdiv_rn(amax, 127.0f);
+        if (t == 0)
+            xs[row] = s;
+        const Quantizer qz(s, ROT);
 #pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        const int64_t idx = t + (int64_t)TPR * j;
-        if (idx < nvec) {
-            float qv[8];
-            if (ROT) {
-                quantize8(qz, v[j], qv);
-            } else {
-                float f[8];
-                unpack8(raw[j], f);
-                quantize8(qz, f, qv);
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t idx = t + (int64_t)TPR * j;
+            if (idx < nvec) {
+                float qv[8];
+                if (ROT) {
+                    quantize8(qz, v[j], qv);
+                } else {
+                    float f[8];
+                    unpack8(raw[j], f);
+                    quantize8(qz, f, qv);
+                }
+                store8<OUT8, OUT16>(qv, q8, q16, row * K + idx * 8);
             }
-            store8<OUT8, OUT16>(qv, q8, q16, row * K + idx * 8);
         }
     }
+    widen_share(w8, w_n16, w16);
 }
 
-// Per-row quantize for rows too long to keep in registers: pass 1 finds the maximum,
-// pass 2 re-reads (from L2) and quantizes.
+// One row of rows_stream_kernel (one warp): pass 1 finds the maximum, pass 2 re-reads
+// (from L2) and quantizes.
 template <bool ROT, bool OUT8, bool OUT16>
-__global__ void __launch_bounds__(THREADS) rows_stream_kernel(const uint4* __restrict__ x, int64_t M, int64_t K,
-                                                              int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
-                                                              float* __restrict__ xs)
+__device__ __forceinline__ void stream_row(const uint4* __restrict__ x, int64_t row, int64_t K, int lane,
+                                           int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
+                                           float* __restrict__ xs)
 {
-    griddep_wait();
-    griddep_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
-    if (row >= M)
-        return;
     const int64_t nvec = K >> 3;
     const uint4* xr = x + row * nvec;
     float amax = 0.0f;
@@ -294,9 +346,27 @@ __global__ void __launch_bounds__(THREADS) rows_stream_kernel(const uint4* __res
     }
 }
 
+// Per-row quantize for rows too long to keep in registers, one warp per row.
+template <bool ROT, bool OUT8, bool OUT16>
+__global__ void __launch_bounds__(THREADS) rows_stream_kernel(const uint4* __restrict__ x, int64_t M, int64_t K,
+                                                              int8_t* __restrict__ q8, __nv_bfloat16* __restrict__ q16,
+                                                              float* __restrict__ xs, const uint4* __restrict__ w8,
+                                                              int64_t w_n16, uint4* __restrict__ w16)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
+    if (row < M)
+        stream_row<ROT, OUT8, OUT16>(x, row, K, lane, q8, q16, xs);
+    widen_share(w8, w_n16, w16);
+}
+
 // Tensorwise pass 1: per-block maximum of |x| over a grid-stride slice.
 __global__ void __launch_bounds__(256) amax_partials_kernel(const uint4* __restrict__ x, int64_t nvec,
-                                                            float* __restrict__ partials)
+                                                            float* __restrict__ partials,
+                                                            const uint4* __restrict__ w8 = nullptr,
+                                                            int64_t w_n16 = 0, uint4* __restrict__ w16 = nullptr)
 {
     griddep_wait();
     griddep_launch_dependents();
@@ -324,6 +394,7 @@ __global__ void __launch_bounds__(256) amax_partials_kernel(const uint4* __restr
         if (threadIdx.x == 0)
             partials[blockIdx.x] = m;
     }
+    widen_share(w8, w_n16, w16);  // a weight widening may share the launch
 }
 
 // Tensorwise pass 2: every block reduces the partial maxima (a few KB, L2 resident),
@@ -377,23 +448,150 @@ __global__ void __launch_bounds__(256) quant_flat_kernel(const uint4* __restrict
     }
 }
 
-// int8 -> bf16 (exact), 16 values per thread and vector.
-__device__ __forceinline__ void widen16(const uint4& v, uint4& lo, uint4& hi)
+// The tensorwise layer's whole preparation in one launch: each block takes the maximum
+// of |x| over its grid-stride slice and publishes it, widens its share of the weight
+// while the other blocks finish, learns the global maximum, and quantizes its slice
+// (re-read from L2) into bf16 codes.
+// Hand-off without atomics or resets: block b writes its maximum into slot b of the
+// caller's workspace and then, with release semantics, this launch's 64-bit epoch next
+// to it; block 0 waits until every slot carries the epoch, reduces the maxima and
+// publishes the result the same way in a final slot, which every other block polls.
+// Values left by any earlier launch carry another epoch and are never taken.  The grid
+// never exceeds the number of co-resident blocks, so every block gets to publish; the
+// waits are bounded all the same (a timeout sets `err` and the block goes on).
+struct alignas(16) EpochSlot {
+    unsigned long long epoch;
+    float value;
+    float pad;
+};
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p)
 {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[8];
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(256) tensorwise_prep_kernel(
+    const uint4* __restrict__ x, int64_t nvec, EpochSlot* slots, unsigned long long epoch,
+    __nv_bfloat16* __restrict__ q16, float* __restrict__ xs, const uint4* __restrict__ w8, int64_t w_n16,
+    uint4* __restrict__ w16, uint64_t timeout_ns, unsigned int* err)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ float red[8];
+    __shared__ float s_amax;
+    __shared__ int s_timeout;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    EpochSlot* done = slots + gridDim.x;
+    // 1. this block's maximum, published
+    __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec; base += UNROLL * stride) {
+        uint4 v[UNROLL];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            v[u] = i < nvec ? ld_stream(x + i) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float a = (float)(int8_t)((w[k] >> (16 * h)) & 0xFFu);
-            const float b = (float)(int8_t)((w[k] >> (16 * h + 8)) & 0xFFu);
-            __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
-            o[2 * k + h] = *reinterpret_cast<uint32_t*>(&p);
+        for (int u = 0; u < UNROLL; ++u)
+            m2 = absmax8(m2, v[u]);
+    }
+    float m = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = m;
+    if (threadIdx.x == 0)
+        s_timeout = 0;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float bm = 0.0f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
+            bm = fmaxf(bm, red[i]);
+        slots[blockIdx.x].value = bm;
+        st_release_u64(&slots[blockIdx.x].epoch, epoch);
+    }
+    // 2. the weight widening hides the wait for the slowest block
+    widen_share(w8, w_n16, w16);
+    // 3. the global maximum
+    if (blockIdx.x == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        m = 0.0f;
+        for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) {
+            uint32_t polls = 0;
+            while (ld_acquire_u64(&slots[i].epoch) != epoch) {
+                if ((++polls & 31u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
+                    s_timeout = 1;
+                    break;
+                }
+            }
+            m = fmaxf(m, __ldcg(&slots[i].value));
+        }
+        m = warp_max(m);
+        if ((threadIdx.x & 31) == 0)
+            red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float g = 0.0f;
+            for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
+                g = fmaxf(g, red[i]);
+            s_amax = g;
+            done->value = g;
+            st_release_u64(&done->epoch, epoch);
+            if (s_timeout)
+                atomicOr(err, kErrWaitGrid);
+        }
+    } else if (threadIdx.x == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        uint32_t polls = 0;
+        while (ld_acquire_u64(&done->epoch) != epoch) {
+            __nanosleep(200);
+            if ((++polls & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
+                atomicOr(err, kErrWaitGrid);
+                break;
+            }
+        }
+        s_amax = __ldcg(&done->value);
+    }
+    __syncthreads();
+    const float sc = __fdiv_rn(s_amax, 127.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        xs[0] = sc;
+    // 4. quantize this block's slice
+    const Quantizer qz(sc, false);
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec; base += UNROLL * stride) {
+        uint4 v[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            v[u] = i < nvec ? ld_stream(x + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            if (i < nvec) {
+                float f[8], qv[8];
+                unpack8(v[u], f);
+                quantize8(qz, f, qv);
+                store8<false, true>(qv, nullptr, q16, i * 8);
+            }
         }
     }
-    lo = make_uint4(o[0], o[1], o[2], o[3]);
-    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Two int8 -> bf16 widenings in one launch (operands of the pre-quantized GEMM entries).
+__global__ void __launch_bounds__(256) widen2_kernel(const uint4* __restrict__ a8, int64_t a_n16,
+                                                     uint4* __restrict__ a16, const uint4* __restrict__ b8,
+                                                     int64_t b_n16, uint4* __restrict__ b16)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    widen_share(a8, a_n16, a16);
+    widen_share(b8, b_n16, b16);
 }
 
 __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ src, int64_t n16,
@@ -401,25 +599,7 @@ __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ sr
 {
     griddep_wait();
     griddep_launch_dependents();
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < n16; base += UNROLL * stride) {
-        uint4 v[UNROLL];
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int64_t i = base + u * stride;
-            v[u] = i < n16 ? ld_stream(src + i) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int64_t i = base + u * stride;
-            if (i < n16) {
-                uint4 lo, hi;
-                widen16(v[u], lo, hi);
-                dst[2 * i] = lo;
-                dst[2 * i + 1] = hi;
-            }
-        }
-    }
+    widen_share(src, n16, dst);
 }
 
 }  // namespace quant
@@ -428,10 +608,13 @@ namespace {
 
 template <bool OUT8, bool OUT16>
 cudaError_t rows_dispatch(const void* x, int64_t M, int64_t K, bool rotate, int8_t* q8, void* q16, float* xs,
-                          cudaStream_t s)
+                          const int8_t* w8_, int64_t w_n, void* w16_, cudaStream_t s)
 {
     using namespace quant;
     const uint4* xv = static_cast<const uint4*>(x);
+    const uint4* w8 = reinterpret_cast<const uint4*>(w8_);
+    uint4* w16 = static_cast<uint4*>(w16_);
+    const int64_t w_n16 = w8 ? (w_n >> 4) : 0;
     __nv_bfloat16* q16b = static_cast<__nv_bfloat16*>(q16);
     const int64_t nvec = K / 8;
     // threads per row: the fewest (32..256) that keep at most 4 vectors per thread,
@@ -449,9 +632,9 @@ cudaError_t rows_dispatch(const void* x, int64_t M, int64_t K, bool rotate, int8
             return cudaErrorInvalidValue;
         if (rotate)
             return launch_pdl(rows_stream_kernel<true, OUT8, OUT16>, (unsigned)blocks, THREADS, 0, s, xv, M, K, q8,
-                              q16b, xs);
+                              q16b, xs, w8, w_n16, w16);
         return launch_pdl(rows_stream_kernel<false, OUT8, OUT16>, (unsigned)blocks, THREADS, 0, s, xv, M, K, q8,
-                          q16b, xs);
+                          q16b, xs, w8, w_n16, w16);
     }
     const int64_t rpb = THREADS / tpr;
     const int64_t blocks = (M + rpb - 1) / rpb;
@@ -459,8 +642,10 @@ cudaError_t rows_dispatch(const void* x, int64_t M, int64_t K, bool rotate, int8
         return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)blocks;
 #define CK_ROWS(T, V)                                                                                   \
-    (rotate ? launch_pdl(rows_kernel<T, V, true, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs) \
-            : launch_pdl(rows_kernel<T, V, false, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs))
+    (rotate ? launch_pdl(rows_kernel<T, V, true, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs, w8, \
+                         w_n16, w16)                                                                 \
+            : launch_pdl(rows_kernel<T, V, false, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs, w8, \
+                         w_n16, w16))
     switch (tpr * 16 + vpt) {
     case 32 * 16 + 4: return CK_ROWS(32, 4);
     case 64 * 16 + 4: return CK_ROWS(64, 4);
@@ -480,8 +665,8 @@ cudaError_t launch_quantize_rows(const void* x, int64_t M, int64_t K, bool rotat
     if (M == 0)
         return cudaSuccess;
     if (q8)
-        return rows_dispatch<true, false>(x, M, K, rotate, q8, q16, x_scale, s);
-    return rows_dispatch<false, true>(x, M, K, rotate, q8, q16, x_scale, s);
+        return rows_dispatch<true, false>(x, M, K, rotate, q8, q16, x_scale, nullptr, 0, nullptr, s);
+    return rows_dispatch<false, true>(x, M, K, rotate, q8, q16, x_scale, nullptr, 0, nullptr, s);
 }
 
 int tensorwise_partials(const DeviceInfo& dev)
@@ -498,7 +683,8 @@ cudaError_t launch_quantize_tensorwise(const void* x, int64_t M, int64_t K, int8
     const int nparts = tensorwise_partials(dev);
     const uint4* xv = static_cast<const uint4*>(x);
     __nv_bfloat16* q16b = static_cast<__nv_bfloat16*>(q16);
-    cudaError_t e = launch_pdl(amax_partials_kernel, nparts, 256, 0, s, xv, nvec, partials);
+    cudaError_t e = launch_pdl(amax_partials_kernel, nparts, 256, 0, s, xv, nvec, partials, (const uint4*)nullptr,
+                               (int64_t)0, (uint4*)nullptr);
     if (e != cudaSuccess)
         return e;
     const int grid = 4 * dev.sm_count;
@@ -519,7 +705,8 @@ cudaError_t launch_quantize_tensorwise_parts(const void* x, int64_t M, int64_t K
     const int64_t nvec = (M * K) >> 3;
     const uint4* xv = static_cast<const uint4*>(x);
     __nv_bfloat16* q16b = static_cast<__nv_bfloat16*>(q16);
-    cudaError_t e = launch_pdl(amax_partials_kernel, nparts, 256, 0, s, xv, nvec, partials);
+    cudaError_t e = launch_pdl(amax_partials_kernel, nparts, 256, 0, s, xv, nvec, partials, (const uint4*)nullptr,
+                               (int64_t)0, (uint4*)nullptr);
     if (e != cudaSuccess)
         return e;
     const int grid = 4 * dev.sm_count;
@@ -542,6 +729,88 @@ cudaError_t launch_widen_int8(const int8_t* src, void* dst, int64_t n, const Dev
     const int grid = (int)(want < cap ? want : cap);
     return launch_pdl(quant::widen_kernel, grid, 256, 0, s, reinterpret_cast<const uint4*>(src), n16,
                       static_cast<uint4*>(dst));
+}
+
+cudaError_t launch_prep_rows(const void* x, int64_t M, int64_t K, bool rotate, void* q16, float* x_scale,
+                             const int8_t* w8, int64_t w_n, void* w16, const DeviceInfo& dev, cudaStream_t s)
+{
+    (void)dev;
+    if (M == 0)
+        return launch_widen_int8(w8, w16, w_n, dev, s);
+    return rows_dispatch<false, true>(x, M, K, rotate, nullptr, q16, x_scale, w8, w_n, w16, s);
+}
+
+namespace {
+
+// Blocks of tensorwise_prep_kernel that are resident at once on the whole device.
+int prep_capacity(const DeviceInfo& dev)
+{
+    static int cached[64] = {};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int& c = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
+    if (c == 0) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant::tensorwise_prep_kernel, 256, 0) !=
+                cudaSuccess ||
+            per_sm <= 0)
+            per_sm = 1;
+        c = per_sm * dev.sm_count;
+    }
+    return c;
+}
+
+// A 64-bit value no earlier launch of this process used (high-entropy start, so values
+// left in recycled memory by another process do not match either).
+unsigned long long next_prep_epoch()
+{
+    static std::atomic<unsigned long long> counter([] {
+        unsigned long long z = (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() ^
+                               ((unsigned long long)getpid() << 29) ^ 0x9E3779B97F4A7C15ull;
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;  // splitmix64 finaliser
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        return z ^ (z >> 31);
+    }());
+    unsigned long long e;
+    do {
+        e = counter.fetch_add(1, std::memory_order_relaxed);
+    } while (e == 0);
+    return e;
+}
+
+}  // namespace
+
+size_t prep_tensorwise_scratch_bytes(int max_blocks)
+{
+    return sizeof(quant::EpochSlot) * (size_t)(max_blocks + 1);
+}
+
+cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q16, float* x_scale, void* scratch,
+                                   int max_blocks, const int8_t* w8, int64_t w_n, void* w16, const DeviceInfo& dev,
+                                   cudaStream_t s)
+{
+    const int64_t nvec = (M * K) >> 3;
+    const int64_t want = std::max<int64_t>(1, (nvec + 255) / 256);
+    const int grid = (int)std::min<int64_t>(std::min<int64_t>(want, prep_capacity(dev)), max_blocks);
+    unsigned int* err = nullptr;
+    cudaError_t e = device_error_ptr(&err);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(quant::tensorwise_prep_kernel, grid, 256, 0, s, static_cast<const uint4*>(x), nvec,
+                      static_cast<quant::EpochSlot*>(scratch), next_prep_epoch(), static_cast<__nv_bfloat16*>(q16),
+                      x_scale, reinterpret_cast<const uint4*>(w8), w_n >> 4, static_cast<uint4*>(w16),
+                      (uint64_t)2000000000ull, err);
+}
+
+cudaError_t launch_widen2(const int8_t* a8, int64_t a_n, void* a16, const int8_t* b8, int64_t b_n, void* b16,
+                          const DeviceInfo& dev, cudaStream_t s)
+{
+    const int64_t n16 = (a_n >> 4) + (b_n >> 4);
+    const int64_t want = std::max<int64_t>(1, (n16 + 1023) / 1024);
+    const int grid = (int)std::min<int64_t>(want, (int64_t)8 * dev.sm_count);
+    return launch_pdl(quant::widen2_kernel, grid, 256, 0, s, reinterpret_cast<const uint4*>(a8), a_n >> 4,
+                      static_cast<uint4*>(a16), reinterpret_cast<const uint4*>(b8), b_n >> 4,
+                      static_cast<uint4*>(b16));
 }
 
 }  // namespace ck

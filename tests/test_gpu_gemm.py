@@ -82,3 +82,16 @@ def test_dequant_parity(M, N, K, scalar, with_bias):
     torch.cuda.synchronize()
     d = bf16_ulp_distance(bits(y), ref)
     assert d.max() <= MAX_ULP, "max ulp %d at %s" % (d.max(), np.unravel_index(d.argmax(), d.shape))
+
+
+@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("bn", [256, 224, 192, 160, 128, 96, 64, 32])
+def test_s32_every_tile_width(monkeypatch, bn, pair):
+    """The tile width is chosen per launch (multiples of 32 up to 256); every width, with
+    CTA pairs and with single CTAs, gives the exact accumulators (ragged M, N and K)."""
+    monkeypatch.setenv("CK_GEMM_BN", str(bn))
+    monkeypatch.setenv("CK_GEMM_PAIR", pair)
+    M, N, K = 300, 712, 1104
+    q = synthetic.int8_uniform((M, K), seed=bn + 1)
+    w = synthetic.int8_uniform((N, K), seed=bn + 2)
+    assert np.array_equal(gpu_acc(q, w), oracle.gemm_s32(q.numpy(), w.numpy()))
