@@ -258,12 +258,13 @@ def run_ours(args, spec):
 
     name, M, N, K, mode, has_bias, frac, seed = spec
     case = synthetic.case_from_spec(spec)
-    if mode == synthetic.CONVROT:
-        raise SystemExit("the ConvRot workload needs its pre-rotated weight from the oracle; bench the "
-                         "per-row or tensorwise workloads")
     x = case.x.to(dev)
-    w = case.w.to(dev)
-    ws_ = case.w_scale.to(dev)
+    if mode == synthetic.CONVROT:
+        # the layer's stored weight W @ H^T, prepared once per layer (not part of a step)
+        w, ws_ = ck.ck_convrot_prepare_weight(case.w_float.to(dev))
+    else:
+        w = case.w.to(dev)
+        ws_ = case.w_scale.to(dev)
     b = None if case.bias is None else case.bias.to(dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     work = ck.workspace(ck.ck_int8_linear_workspace_size(M, N, K, mode), dev)

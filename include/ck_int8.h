@@ -118,6 +118,17 @@ size_t ck_int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
 int ck_int8_linear(const void *x, const int8_t *w, const float *w_scale, const void *bias, void *y, int64_t M,
                    int64_t N, int64_t K, int mode, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ConvRot weight preparation (issue #278, "Suggested fix": the stored weight is
+ * W_rot = W @ H^T; since H is symmetric, row n of it is row n of W times H), quantized
+ * per output row, once per layer:
+ *   W:       fp32 [N,K] device, read only; K % 128 == 0.
+ *   w:       int8 [N,K] device, written: clamp(rint(v / w_scale[n]), -127, 127) with v the
+ *            rotated row (the same fp32 block transform as ck_quantize_int8_rowwise's
+ *            rotation), one IEEE fp32 division, rint half to even.
+ *   w_scale: fp32 [N] device, written: max_k |v[n,k]| / 127.
+ * The result is the w / w_scale that ck_int8_linear takes in CK_CONVROT mode. */
+int ck_convrot_prepare_weight(const float *W, int64_t N, int64_t K, int8_t *w, float *w_scale, void *stream);
+
 /* GEMM + fused dequant on an already-quantized activation (the second half of
  * ck_int8_linear): q int8 [M,K], x_scale fp32 [M] (or [1] if scalar_scales), w int8
  * [N,K], w_scale fp32 [N] (or [1]), bias bf16 [N] or NULL, y bf16 [M,N].

@@ -47,6 +47,7 @@ def load_library(path=None):
         "ck_quantize_int8_tensorwise_noalloc": ([P, I64, I64, P, P, P], I),
         "ck_int8_linear_workspace_size": ([I64, I64, I64, I], SZ),
         "ck_int8_linear": ([P, P, P, P, P, I64, I64, I64, I, P, SZ, P], I),
+        "ck_convrot_prepare_weight": ([P, I64, I64, P, P, P], I),
         "ck_int8_gemm_workspace_size": ([I64, I64, I64], SZ),
         "ck_int8_gemm_dequant": ([P, P, P, P, P, P, I64, I64, I64, I, P, SZ, P], I),
         "ck_int8_gemm_s32": ([P, P, P, I64, I64, I64, P, SZ, P], I),
@@ -166,6 +167,18 @@ def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stre
     _check(L.ck_int8_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, int(mode), _ptr(ws),
                             ws.numel(), _stream(stream)))
     return y
+
+
+def ck_convrot_prepare_weight(W, w=None, w_scale=None, stream=None):
+    """ConvRot weight: fp32 W [N,K] -> (int8 codes of W @ H^T [N,K], fp32 row scales [N])."""
+    N, K = W.shape
+    _req(W, torch.float32, (N, K), "W")
+    w = torch.empty((N, K), dtype=torch.int8, device=W.device) if w is None else w
+    w_scale = torch.empty((N,), dtype=torch.float32, device=W.device) if w_scale is None else w_scale
+    _req(w, torch.int8, (N, K), "w")
+    _req(w_scale, torch.float32, (N,), "w_scale")
+    _check(load_library().ck_convrot_prepare_weight(_ptr(W), N, K, _ptr(w), _ptr(w_scale), _stream(stream)))
+    return w, w_scale
 
 
 def ck_int8_gemm_dequant(q, x_scale, w, w_scale, bias=None, scalar_scales=False, y=None, ws=None, stream=None):

@@ -366,6 +366,28 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
     return CK_OK;
 }
 
+int ck_convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8_t* w, float* w_scale, void* stream)
+{
+    if (N < 0 || K <= 0)
+        return fail(CK_ERR_INVALID_ARG, "N must be >= 0 and K >= 1 (got N=%lld K=%lld)", (long long)N, (long long)K);
+    if (K % 128 != 0)
+        return fail(CK_ERR_INVALID_ARG, "the ConvRot rotation needs K % 128 == 0 (got %lld)", (long long)K);
+    if (N > kMaxDim)
+        return fail(CK_ERR_INVALID_ARG, "N must be < 2^31 (got %lld)", (long long)N);
+    if (N == 0)
+        return CK_OK;
+    CK_REQUIRE_PTR(W);
+    CK_REQUIRE_PTR(w);
+    CK_REQUIRE_PTR(w_scale);
+    DeviceInfo dev;
+    int st = check_device(&dev);
+    if (st != CK_OK)
+        return st;
+    log_shape("convrot_prepare_weight", 0, N, K, CK_CONVROT, "rows-fwht");
+    cudaError_t e = launch_convrot_weight(W, N, K, w, w_scale, dev, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CK_OK : cuda_fail(e, "ck_convrot_prepare_weight launch");
+}
+
 size_t ck_int8_gemm_workspace_size(int64_t M, int64_t N, int64_t K)
 {
     if (M < 0 || N < 0 || K < 0)

@@ -85,6 +85,9 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
 // Two int8 -> bf16 widenings in one launch.
 cudaError_t launch_widen2(const int8_t* a8, int64_t a_n, void* a16, const int8_t* b8, int64_t b_n, void* b16,
                           const DeviceInfo& dev, cudaStream_t s);
+// ConvRot weight preparation: W fp32 [N,K] -> int8 codes of W @ H^T and fp32 row scales.
+cudaError_t launch_convrot_weight(const float* W, int64_t N, int64_t K, int8_t* w, float* w_scale,
+                                  const DeviceInfo& dev, cudaStream_t s);
 // Device address of the library's error word on the current device.
 cudaError_t device_error_ptr(unsigned int** ptr);
 // int8 -> bf16 widening of n values (n % 16 == 0).

@@ -362,6 +362,122 @@ __global__ void __launch_bounds__(THREADS) rows_stream_kernel(const uint4* __res
     widen_share(w8, w_n16, w16);
 }
 
+// ConvRot weight preparation (issue #278, "Suggested fix": the stored weight is
+// W_rot = W @ H^T, quantized per output row).  H is symmetric, so row n of W @ H^T is row
+// n of W times H: the block transform of the activations, applied to fp32 rows.  Then
+// w_scale[n] = max|W_rot[n]| / 127 and w = clamp(rint(W_rot / w_scale), -127, 127), with
+// the IEEE division (fp32 input).  A vector slot here is 8 fp32 values (two 16-byte loads).
+__device__ __forceinline__ void load8_f32(const float4* __restrict__ p, int64_t idx, bool valid, float (&f)[8])
+{
+    if (valid) {
+        const float4 a = __ldg(p + 2 * idx), b = __ldg(p + 2 * idx + 1);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            f[i] = 0.0f;
+    }
+}
+
+template <int TPR, int VPT>
+__global__ void __launch_bounds__(THREADS) weight_rot_kernel(const float4* __restrict__ W, int64_t N, int64_t K,
+                                                             int8_t* __restrict__ w, float* __restrict__ ws)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    constexpr int RPB = THREADS / TPR;
+    constexpr int WPR = TPR / 32;
+    __shared__ float red[THREADS / 32];
+    const int lane = threadIdx.x & 31;
+    const int t = threadIdx.x % TPR;
+    const int g = threadIdx.x / TPR;
+    const int64_t row = (int64_t)blockIdx.x * RPB + g;
+    const bool live = row < N;
+    const int64_t nvec = K >> 3;
+    const float4* wr = W + (live ? row : 0) * (nvec * 2);
+    const int64_t warp_first = t - lane;
+    float v[VPT][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t idx = t + (int64_t)TPR * j;
+        load8_f32(wr, idx, live && idx < nvec, v[j]);
+        if (warp_first + (int64_t)TPR * j < nvec) {  // warp-uniform
+            fwht_slot(v[j], lane);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                amax = fmaxf(amax, fabsf(v[j][e]));
+        }
+    }
+    amax = warp_max(amax);
+    if (WPR > 1) {
+        if (lane == 0)
+            red[threadIdx.x >> 5] = amax;
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < WPR; ++i)
+            amax = fmaxf(amax, red[g * WPR + i]);
+    }
+    if (!live)
+        return;
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (t == 0)
+        ws[row] = s;
+    const Quantizer qz(s, true);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t idx = t + (int64_t)TPR * j;
+        if (idx < nvec) {
+            float qv[8];
+            quantize8(qz, v[j], qv);
+            store8<true, false>(qv, w, nullptr, row * K + idx * 8);
+        }
+    }
+}
+
+// The same for rows longer than 16384 values: one warp per row, two passes.
+__global__ void __launch_bounds__(THREADS) weight_rot_stream_kernel(const float4* __restrict__ W, int64_t N,
+                                                                    int64_t K, int8_t* __restrict__ w,
+                                                                    float* __restrict__ ws)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
+    if (row >= N)
+        return;  // the whole warp leaves together
+    const int64_t nvec = K >> 3;
+    const float4* wr = W + row * (nvec * 2);
+    float amax = 0.0f;
+    for (int64_t base = 0; base < nvec; base += 32) {
+        const int64_t idx = base + lane;
+        float f[8];
+        load8_f32(wr, idx, idx < nvec, f);
+        fwht_slot(f, lane);
+        if (idx < nvec) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                amax = fmaxf(amax, fabsf(f[e]));
+        }
+    }
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (lane == 0)
+        ws[row] = s;
+    const Quantizer qz(s, true);
+    for (int64_t base = 0; base < nvec; base += 32) {
+        const int64_t idx = base + lane;
+        float f[8], qv[8];
+        load8_f32(wr, idx, idx < nvec, f);
+        fwht_slot(f, lane);
+        if (idx < nvec) {
+            quantize8(qz, f, qv);
+            store8<true, false>(qv, w, nullptr, row * K + idx * 8);
+        }
+    }
+}
+
 // Tensorwise pass 1: per-block maximum of |x| over a grid-stride slice.
 __global__ void __launch_bounds__(256) amax_partials_kernel(const uint4* __restrict__ x, int64_t nvec,
                                                             float* __restrict__ partials,
@@ -811,6 +927,41 @@ cudaError_t launch_widen2(const int8_t* a8, int64_t a_n, void* a16, const int8_t
     return launch_pdl(quant::widen2_kernel, grid, 256, 0, s, reinterpret_cast<const uint4*>(a8), a_n >> 4,
                       static_cast<uint4*>(a16), reinterpret_cast<const uint4*>(b8), b_n >> 4,
                       static_cast<uint4*>(b16));
+}
+
+cudaError_t launch_convrot_weight(const float* W, int64_t N, int64_t K, int8_t* w, float* w_scale,
+                                  const DeviceInfo& dev, cudaStream_t s)
+{
+    (void)dev;
+    using namespace quant;
+    if (N == 0)
+        return cudaSuccess;
+    const float4* Wv = reinterpret_cast<const float4*>(W);
+    const int64_t nvec = K / 8;
+    int tpr, vpt;
+    if (nvec <= 128) { tpr = 32; vpt = 4; }
+    else if (nvec <= 256) { tpr = 64; vpt = 4; }
+    else if (nvec <= 512) { tpr = 128; vpt = 4; }
+    else if (nvec <= 1024) { tpr = 256; vpt = 4; }
+    else if (nvec <= 2048) { tpr = 256; vpt = 8; }
+    else { tpr = 0; vpt = 0; }
+    if (tpr == 0) {
+        const int64_t blocks = (N + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
+        if (blocks > 0x7FFFFFFF)
+            return cudaErrorInvalidValue;
+        return launch_pdl(weight_rot_stream_kernel, (unsigned)blocks, THREADS, 0, s, Wv, N, K, w, w_scale);
+    }
+    const int64_t blocks = (N + THREADS / tpr - 1) / (THREADS / tpr);
+    if (blocks > 0x7FFFFFFF)
+        return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)blocks;
+    switch (tpr * 16 + vpt) {
+    case 32 * 16 + 4: return launch_pdl(weight_rot_kernel<32, 4>, grid, THREADS, 0, s, Wv, N, K, w, w_scale);
+    case 64 * 16 + 4: return launch_pdl(weight_rot_kernel<64, 4>, grid, THREADS, 0, s, Wv, N, K, w, w_scale);
+    case 128 * 16 + 4: return launch_pdl(weight_rot_kernel<128, 4>, grid, THREADS, 0, s, Wv, N, K, w, w_scale);
+    case 256 * 16 + 4: return launch_pdl(weight_rot_kernel<256, 4>, grid, THREADS, 0, s, Wv, N, K, w, w_scale);
+    default: return launch_pdl(weight_rot_kernel<256, 8>, grid, THREADS, 0, s, Wv, N, K, w, w_scale);
+    }
 }
 
 }  // namespace ck

@@ -96,3 +96,24 @@ def test_empty_batch_is_a_no_op():
     q, s = ck.ck_quantize_int8_rowwise(x)
     torch.cuda.synchronize()
     assert q.shape == (0, 64) and s.shape == (0,)
+
+
+@pytest.mark.parametrize("N,K", [(12288, 3072), (5, 128), (33, 16384), (3, 16512), (7, 4224), (256, 512)])
+def test_convrot_weight_preparation_parity(N, K):
+    """W fp32 -> int8 codes of W @ H^T and fp32 row scales, bit-exact with the oracle's
+    preparation (the ConvRot workload's weight is the first shape)."""
+    W = synthetic.normal_f32((N, K), seed=N + K, std=0.02)
+    w_ref, s_ref = oracle.prepare_convrot_weight(W.numpy())
+    w, s = ck.ck_convrot_prepare_weight(W.to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    wn = w.cpu().numpy()
+    bad = np.argwhere(wn != w_ref)
+    assert bad.size == 0, "%d codes differ, first %s" % (len(bad), bad[0])
+
+
+def test_convrot_weight_preparation_rejects_unaligned_k():
+    W = torch.zeros((4, 200), dtype=torch.float32, device=DEV)
+    with pytest.raises(ck.CkError) as e:
+        ck.ck_convrot_prepare_weight(W)
+    assert "128" in str(e.value)
