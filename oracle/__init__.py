@@ -32,6 +32,10 @@ def lib():
         L.ck_oracle_gemm_s32.restype = ctypes.c_int
         L.ck_oracle_dequant.argtypes = [P, P, P, P, ctypes.c_int, I64, I64, P]
         L.ck_oracle_dequant.restype = None
+        L.ck_oracle_dequant_typed.argtypes = [P, P, P, P, ctypes.c_int, I64, I64, ctypes.c_int, P]
+        L.ck_oracle_dequant_typed.restype = None
+        L.ck_oracle_f32_to_f16.argtypes = [ctypes.c_float]
+        L.ck_oracle_f32_to_f16.restype = ctypes.c_uint16
         L.ck_oracle_int8_linear.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_int, P, P, P, P]
         L.ck_oracle_int8_linear.restype = ctypes.c_int
         L.ck_oracle_fwht128.argtypes = [P]
@@ -147,7 +151,33 @@ def dequant(acc, xs, ws, bias_bits=None, scalar_scales=False):
     return y
 
 
-def int8_linear(x_bits, w, ws, bias_bits=None, mode=PER_ROW):
+OUT_BF16, OUT_F16, OUT_F32 = 0, 1, 2
+
+
+def f32_to_f16(vals):
+    """float32 -> IEEE half bits with the oracle's round-to-nearest-even."""
+    vals = _c(vals, np.float32)
+    out = np.empty(vals.shape, np.uint16)
+    L = lib()
+    for i, v in enumerate(vals.reshape(-1)):
+        out.reshape(-1)[i] = L.ck_oracle_f32_to_f16(float(v))
+    return out
+
+
+def dequant_typed(acc, xs, ws, bias_bits=None, scalar_scales=False, out_dtype=OUT_BF16):
+    """fp32 epilogue -> bf16 bits / fp16 bits (uint16) or fp32 values [M,N]."""
+    acc = _c(acc, np.int32)
+    xs = _c(xs, np.float32)
+    ws = _c(ws, np.float32)
+    b = None if bias_bits is None else _c(bias_bits, np.uint16)
+    M, N = acc.shape
+    y = np.empty((M, N), np.float32 if out_dtype == OUT_F32 else np.uint16)
+    lib().ck_oracle_dequant_typed(_p(acc), _p(xs), _p(ws), _p(b), int(bool(scalar_scales)), M, N, int(out_dtype),
+                                  _p(y))
+    return y
+
+
+def int8_linear(x_bits, w, ws, bias_bits=None, mode=PER_ROW, out_dtype=OUT_BF16):
     """Whole layer; returns dict(y=bf16 bits [M,N], q, xs, acc)."""
     x = _c(x_bits, np.uint16)
     w = _c(w, np.int8)
@@ -163,6 +193,8 @@ def int8_linear(x_bits, w, ws, bias_bits=None, mode=PER_ROW):
                                      _p(y), _p(q), _p(xs), _p(acc))
     if rc != 0:
         raise ValueError("oracle int8_linear failed (rc=%d)" % rc)
+    if out_dtype != OUT_BF16:
+        y = dequant_typed(acc, xs, ws, b, scalar_scales=(mode == TENSORWISE), out_dtype=out_dtype)
     return {"y": y, "q": q, "xs": xs, "acc": acc}
 
 

@@ -70,7 +70,44 @@ static uint16_t f32_to_bf16_bits_rne(float f)
     return (uint16_t)(u >> 16);
 }
 
+/* round-to-nearest-even of an fp32 to IEEE binary16 (finite inputs; overflow gives
+ * +-infinity, values below the smallest subnormal round to +-0 or the smallest one) */
+static uint16_t f32_to_f16_bits_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    const uint32_t sign = (u >> 16) & 0x8000u;
+    const uint32_t mag = u & 0x7FFFFFFFu;
+    if (mag >= 0x47800000u) {          /* |f| >= 65536: overflow (65520 and up round here too) */
+        return (uint16_t)(sign | 0x7C00u);
+    }
+    if (mag >= 0x38800000u) {          /* |f| >= 2^-14: normal half */
+        uint32_t exp = (mag >> 23) - 127 + 15;
+        uint32_t man = mag & 0x7FFFFFu;
+        uint32_t h = (exp << 10) | (man >> 13);
+        uint32_t rem = man & 0x1FFFu;  /* 13 dropped bits */
+        if (rem > 0x1000u || (rem == 0x1000u && (h & 1u)))
+            h += 1;                    /* may carry into the exponent: still correct, 0x7C00 = inf */
+        return (uint16_t)(sign | h);
+    }
+    /* subnormal half: value = m * 2^-24 with m in [0, 1023] */
+    {
+        int e = (int)(mag >> 23);      /* biased fp32 exponent */
+        if (e < 102)                   /* |f| < 2^-25: rounds to zero */
+            return (uint16_t)sign;
+        uint32_t man = (mag & 0x7FFFFFu) | 0x800000u;  /* 24-bit significand, value man * 2^(e-150) */
+        int shift = 126 - e;           /* man * 2^(e-150) / 2^-24 = man >> (126 - e) */
+        uint32_t h = man >> shift;
+        uint32_t rem = man & ((1u << shift) - 1u);
+        uint32_t halfway = 1u << (shift - 1);
+        if (rem > halfway || (rem == halfway && (h & 1u)))
+            h += 1;
+        return (uint16_t)(sign | h);
+    }
+}
+
 /* exported for the pins: the same conversions, callable from tests */
+uint16_t ck_oracle_f32_to_f16(float f) { return f32_to_f16_bits_rne(f); }
 float ck_oracle_bf16_to_f32(uint16_t h) { return bf16_bits_to_f32(h); }
 uint16_t ck_oracle_f32_to_bf16(float f) { return f32_to_bf16_bits_rne(f); }
 
@@ -229,6 +266,32 @@ void ck_oracle_dequant(const int32_t *acc, const float *xs, const float *ws, con
             if (bias)
                 t = t + bf16_bits_to_f32(bias[n]);
             y[m * N + n] = f32_to_bf16_bits_rne(t);
+        }
+    }
+}
+
+/* The same epilogue with the output type of the pages' int8_linear(..., out_dtype):
+ * out_dtype 0 = bf16, 1 = fp16, 2 = fp32; y holds M*N values of that type.  The fp32
+ * value t is the same in every case; only the final rounding differs (none for fp32). */
+void ck_oracle_dequant_typed(const int32_t *acc, const float *xs, const float *ws, const uint16_t *bias,
+                             int scalar_scales, int64_t M, int64_t N, int out_dtype, void *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++) {
+        float xsm = scalar_scales ? xs[0] : xs[m];
+        for (int64_t n = 0; n < N; n++) {
+            float wsn = scalar_scales ? ws[0] : ws[n];
+            float t = (float)acc[m * N + n];
+            t = t * xsm;
+            t = t * wsn;
+            if (bias)
+                t = t + bf16_bits_to_f32(bias[n]);
+            if (out_dtype == 2)
+                ((float *)y)[m * N + n] = t;
+            else if (out_dtype == 1)
+                ((uint16_t *)y)[m * N + n] = f32_to_f16_bits_rne(t);
+            else
+                ((uint16_t *)y)[m * N + n] = f32_to_bf16_bits_rne(t);
         }
     }
 }

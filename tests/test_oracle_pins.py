@@ -182,6 +182,44 @@ def test_bf16_rounding_matches_torch():
     assert np.array_equal(mine, ref)
 
 
+def test_f16_rounding_matches_numpy():
+    rng = np.random.default_rng(18)
+    v = np.concatenate([
+        (rng.standard_normal(4000) * 10.0 ** rng.integers(-9, 6, 4000)).astype(np.float32),
+        np.array([65504.0, 65519.9, 65520.0, 70000.0, -65520.0, 2.0 ** -14, 2.0 ** -24, 2.0 ** -25,
+                  2.0 ** -25 * 1.0000001, 3 * 2.0 ** -26, 1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 0.0, -0.0,
+                  5.960464477539063e-08, 6.097555160522461e-05, 1e-8], np.float32)]).astype(np.float32)
+    mine = oracle.f32_to_f16(v)
+    ref = v.astype(np.float16).view(np.uint16)
+    bad = np.nonzero(mine != ref)[0]
+    assert bad.size == 0, [(float(v[i]), hex(mine[i]), hex(ref[i])) for i in bad[:5]]
+
+
+@pytest.mark.parametrize("out_dtype", [oracle.OUT_F16, oracle.OUT_F32])
+def test_dequant_typed_outputs_share_the_fp32_value(out_dtype):
+    rng = np.random.default_rng(19)
+    acc = rng.integers(-10 ** 6, 10 ** 6, size=(6, 16), dtype=np.int64).astype(np.int32)
+    xs = (rng.random(6) * 1e-3).astype(np.float32)
+    ws = (rng.random(16) * 1e-2).astype(np.float32)
+    b = to_bf16_bits(rng.standard_normal(16) * 0.1)
+    f32 = oracle.dequant_typed(acc, xs, ws, b, out_dtype=oracle.OUT_F32)
+    # the fp32 output is the epilogue value itself: bf16 and fp16 are its roundings
+    assert np.array_equal(oracle.dequant_typed(acc, xs, ws, b, out_dtype=oracle.OUT_BF16),
+                          bits(torch.from_numpy(f32).to(torch.bfloat16)))
+    if out_dtype == oracle.OUT_F16:
+        assert np.array_equal(oracle.dequant_typed(acc, xs, ws, b, out_dtype=out_dtype),
+                              f32.astype(np.float16).view(np.uint16))
+    # and it is within its rounding bound of the exact value
+    for m in range(6):
+        for n in range(16):
+            prod = Fraction(int(acc[m, n])) * Fraction(float(xs[m])) * Fraction(float(ws[n]))
+            bias = Fraction(float(oracle.bf16_to_f32(b[n:n + 1])[0]))
+            # three fp32 roundings, each at most half an ulp of an intermediate bounded by
+            # the operands' magnitudes (the sum may cancel)
+            bound = (abs(prod) + abs(bias)) * Fraction(4, 2 ** 24)
+            assert abs(Fraction(float(f32[m, n])) - (prod + bias)) <= bound
+
+
 def test_dequant_hand_example():
     acc = np.array([[1000, -3, 0, 7]], np.int32)
     xs = np.array([0.5], np.float32)
