@@ -1,7 +1,7 @@
 /*
  * ck_int8.h -- C ABI of the INT8 quantized linear layer for one NVIDIA GB300 (sm_103a).
  *
- *   y[m,n] = bf16( float(acc[m,n]) * x_scale[m] * w_scale[n] (+ bias[n]) )
+ *   y[m,n] = out( float(acc[m,n]) * x_scale[m] * w_scale[n] (+ bias[n]) ),  out = bf16, fp16 or fp32
  *   acc[m,n] = sum_k q[m,k] * w[n,k]            exact int32
  *   q = clamp(rint(v / x_scale), -127, 127),  x_scale = max|v| / 127
  *   v = x (TENSORWISE, PER_ROW) or x @ H (CONVROT)
@@ -55,6 +55,15 @@ typedef enum {
     CK_PER_ROW = 1,    /* x_scale per activation row, w_scale per output channel     */
     CK_CONVROT = 2     /* like CK_PER_ROW on x @ H; w is the pre-rotated W @ H^T      */
 } ck_mode_t;
+
+/* Output element type of the dequant epilogue (the out_dtype of int8_linear).  The fp32
+ * value is the same for every type; bf16 and fp16 round it to nearest even (fp16
+ * overflows to +-inf, keeps subnormals); fp32 stores it as is. */
+typedef enum {
+    CK_OUT_BF16 = 0,
+    CK_OUT_F16 = 1,
+    CK_OUT_F32 = 2
+} ck_dtype_t;
 
 typedef enum {
     CK_OK = 0,
@@ -111,12 +120,15 @@ size_t ck_int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
  *            the pre-rotated, per-row quantized W @ H^T, used as is.
  *   w_scale: fp32 [N] (CK_PER_ROW, CK_CONVROT) or fp32 [1] (CK_TENSORWISE).
  *   bias:    bf16 [N] or NULL.
- *   y:       bf16 [M,N], written.  y = bf16_rne(((float(acc) * xs) * ws) + bias) with
- *            every fp32 operation rounded separately, in that order.
+ *   y:       [M,N] of out_dtype (a ck_dtype_t), written.
+ *            y = out(((float(acc) * xs) * ws) + bias) with every fp32 operation rounded
+ *            separately, in that order, and out the rounding of ck_dtype_t.
  *   workspace/workspace_bytes: device scratch of ck_int8_linear_workspace_size() bytes.
- * No int32 intermediate is ever written to device memory. */
+ * No int32 intermediate is ever written to device memory.  An out_dtype outside
+ * ck_dtype_t gives CK_ERR_INVALID_ARG. */
 int ck_int8_linear(const void *x, const int8_t *w, const float *w_scale, const void *bias, void *y, int64_t M,
-                   int64_t N, int64_t K, int mode, void *workspace, size_t workspace_bytes, void *stream);
+                   int64_t N, int64_t K, int mode, int out_dtype, void *workspace, size_t workspace_bytes,
+                   void *stream);
 
 /* ConvRot weight preparation (issue #278, "Suggested fix": the stored weight is
  * W_rot = W @ H^T; since H is symmetric, row n of it is row n of W times H), quantized
@@ -131,12 +143,12 @@ int ck_convrot_prepare_weight(const float *W, int64_t N, int64_t K, int8_t *w, f
 
 /* GEMM + fused dequant on an already-quantized activation (the second half of
  * ck_int8_linear): q int8 [M,K], x_scale fp32 [M] (or [1] if scalar_scales), w int8
- * [N,K], w_scale fp32 [N] (or [1]), bias bf16 [N] or NULL, y bf16 [M,N].
- * workspace: ck_int8_gemm_workspace_size(M, N, K) bytes. */
+ * [N,K], w_scale fp32 [N] (or [1]), bias bf16 [N] or NULL, y [M,N] of out_dtype
+ * (a ck_dtype_t).  workspace: ck_int8_gemm_workspace_size(M, N, K) bytes. */
 size_t ck_int8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 int ck_int8_gemm_dequant(const int8_t *q, const float *x_scale, const int8_t *w, const float *w_scale,
                          const void *bias, void *y, int64_t M, int64_t N, int64_t K, int scalar_scales,
-                         void *workspace, size_t workspace_bytes, void *stream);
+                         int out_dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /* The raw int32 accumulators acc[m,n] = sum_k q[m,k] w[n,k] of the same GEMM engine,
  * written to acc int32 [M,N] (for exactness checks; the fused path never writes them).

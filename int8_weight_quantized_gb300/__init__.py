@@ -15,6 +15,9 @@ import torch
 from . import build as _build
 
 TENSORWISE, PER_ROW, CONVROT = 0, 1, 2
+OUT_BF16, OUT_F16, OUT_F32 = 0, 1, 2
+# output element type of the dequant epilogue, by torch dtype
+OUT_DTYPES = {torch.bfloat16: OUT_BF16, torch.float16: OUT_F16, torch.float32: OUT_F32}
 CK_OK, CK_ERR_INVALID_ARG, CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA, CK_ERR_TIMEOUT = range(5)
 STATUS_NAMES = {0: "CK_OK", 1: "CK_ERR_INVALID_ARG", 2: "CK_ERR_UNSUPPORTED_DEVICE", 3: "CK_ERR_CUDA",
                 4: "CK_ERR_TIMEOUT"}
@@ -46,10 +49,10 @@ def load_library(path=None):
         "ck_quantize_int8_tensorwise": ([P, I64, I64, P, P, P, SZ, P], I),
         "ck_quantize_int8_tensorwise_noalloc": ([P, I64, I64, P, P, P], I),
         "ck_int8_linear_workspace_size": ([I64, I64, I64, I], SZ),
-        "ck_int8_linear": ([P, P, P, P, P, I64, I64, I64, I, P, SZ, P], I),
+        "ck_int8_linear": ([P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_convrot_prepare_weight": ([P, I64, I64, P, P, P], I),
         "ck_int8_gemm_workspace_size": ([I64, I64, I64], SZ),
-        "ck_int8_gemm_dequant": ([P, P, P, P, P, P, I64, I64, I64, I, P, SZ, P], I),
+        "ck_int8_gemm_dequant": ([P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_int8_gemm_s32": ([P, P, P, I64, I64, I64, P, SZ, P], I),
         "ck_profile_begin": ([I], I),
         "ck_profile_end": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I], I),
@@ -150,8 +153,15 @@ def ck_int8_linear_workspace_size(M, N, K, mode):
     return load_library().ck_int8_linear_workspace_size(M, N, K, int(mode))
 
 
-def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stream=None):
-    """y [M,N] bf16 = dequant(int32 GEMM(quantize(x [@ H]), w)) (+ bias)."""
+def _out_code(out_dtype):
+    if out_dtype not in OUT_DTYPES:
+        raise ValueError("out_dtype must be torch.bfloat16, torch.float16 or torch.float32, got %s" % (out_dtype,))
+    return OUT_DTYPES[out_dtype]
+
+
+def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stream=None, out_dtype=torch.bfloat16):
+    """y [M,N] of out_dtype = dequant(int32 GEMM(quantize(x [@ H]), w)) (+ bias)."""
+    code = _out_code(out_dtype)
     M, K = x.shape
     N = w.shape[0]
     _req(x, torch.bfloat16, (M, K), "x")
@@ -159,13 +169,13 @@ def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stre
     _req(w_scale, torch.float32, (1,) if mode == TENSORWISE else (N,), "w_scale")
     if bias is not None:
         _req(bias, torch.bfloat16, (N,), "bias")
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if y is None else y
-    _req(y, torch.bfloat16, (M, N), "y")
+    y = torch.empty((M, N), dtype=out_dtype, device=x.device) if y is None else y
+    _req(y, out_dtype, (M, N), "y")
     L = load_library()
     need = L.ck_int8_linear_workspace_size(M, N, K, int(mode))
     ws = workspace(need, x.device) if ws is None else ws
-    _check(L.ck_int8_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, int(mode), _ptr(ws),
-                            ws.numel(), _stream(stream)))
+    _check(L.ck_int8_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, int(mode), code,
+                            _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 
@@ -181,8 +191,10 @@ def ck_convrot_prepare_weight(W, w=None, w_scale=None, stream=None):
     return w, w_scale
 
 
-def ck_int8_gemm_dequant(q, x_scale, w, w_scale, bias=None, scalar_scales=False, y=None, ws=None, stream=None):
-    """GEMM + fused dequant on pre-quantized q int8 [M,K]; returns y bf16 [M,N]."""
+def ck_int8_gemm_dequant(q, x_scale, w, w_scale, bias=None, scalar_scales=False, y=None, ws=None, stream=None,
+                         out_dtype=torch.bfloat16):
+    """GEMM + fused dequant on pre-quantized q int8 [M,K]; returns y [M,N] of out_dtype."""
+    code = _out_code(out_dtype)
     M, K = q.shape
     N = w.shape[0]
     _req(q, torch.int8, (M, K), "q")
@@ -191,13 +203,13 @@ def ck_int8_gemm_dequant(q, x_scale, w, w_scale, bias=None, scalar_scales=False,
     _req(w_scale, torch.float32, (1,) if scalar_scales else (N,), "w_scale")
     if bias is not None:
         _req(bias, torch.bfloat16, (N,), "bias")
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=q.device) if y is None else y
-    _req(y, torch.bfloat16, (M, N), "y")
+    y = torch.empty((M, N), dtype=out_dtype, device=q.device) if y is None else y
+    _req(y, out_dtype, (M, N), "y")
     L = load_library()
     need = L.ck_int8_gemm_workspace_size(M, N, K)
     ws = workspace(need, q.device) if ws is None else ws
     _check(L.ck_int8_gemm_dequant(_ptr(q), _ptr(x_scale), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K,
-                                  int(bool(scalar_scales)), _ptr(ws), ws.numel(), _stream(stream)))
+                                  int(bool(scalar_scales)), code, _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 

@@ -303,11 +303,19 @@ size_t ck_int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode)
     return linear_ws_bytes(M, N, K, mode, kMaxPartials);
 }
 
+static bool valid_out_dtype(int t)
+{
+    return t == CK_OUT_BF16 || t == CK_OUT_F16 || t == CK_OUT_F32;
+}
+
 int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const void* bias, void* y, int64_t M,
-                   int64_t N, int64_t K, int mode, void* workspace, size_t workspace_bytes, void* stream)
+                   int64_t N, int64_t K, int mode, int out_dtype, void* workspace, size_t workspace_bytes,
+                   void* stream)
 {
     if (mode != CK_TENSORWISE && mode != CK_PER_ROW && mode != CK_CONVROT)
         return fail(CK_ERR_INVALID_ARG, "mode must be 0 (tensorwise), 1 (per-row) or 2 (ConvRot), got %d", mode);
+    if (!valid_out_dtype(out_dtype))
+        return fail(CK_ERR_INVALID_ARG, "out_dtype must be 0 (bf16), 1 (fp16) or 2 (fp32), got %d", out_dtype);
     int st = check_gemm_shape(M, N, K);
     if (st != CK_OK)
         return st;
@@ -356,6 +364,7 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
     p.bias = bias;
     p.scalar_scales = mode == CK_TENSORWISE;
     p.y = y;
+    p.out_dtype = out_dtype;
     std::string why;
     {
         ProfScope ps(kProfGemm, 1, s);
@@ -396,9 +405,11 @@ size_t ck_int8_gemm_workspace_size(int64_t M, int64_t N, int64_t K)
 }
 
 static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, const float* w_scale, const void* bias,
-                      void* y, int32_t* acc, int64_t M, int64_t N, int64_t K, int scalar_scales, void* workspace,
-                      size_t workspace_bytes, void* stream, const char* name)
+                      void* y, int32_t* acc, int64_t M, int64_t N, int64_t K, int scalar_scales, int out_dtype,
+                      void* workspace, size_t workspace_bytes, void* stream, const char* name)
 {
+    if (acc == nullptr && !valid_out_dtype(out_dtype))
+        return fail(CK_ERR_INVALID_ARG, "out_dtype must be 0 (bf16), 1 (fp16) or 2 (fp32), got %d", out_dtype);
     int st = check_gemm_shape(M, N, K);
     if (st != CK_OK)
         return st;
@@ -447,6 +458,7 @@ static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, co
     p.bias = bias;
     p.scalar_scales = scalar_scales != 0;
     p.y = acc ? nullptr : y;
+    p.out_dtype = out_dtype;
     p.acc = acc;
     std::string why;
     {
@@ -460,17 +472,17 @@ static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, co
 
 int ck_int8_gemm_dequant(const int8_t* q, const float* x_scale, const int8_t* w, const float* w_scale,
                          const void* bias, void* y, int64_t M, int64_t N, int64_t K, int scalar_scales,
-                         void* workspace, size_t workspace_bytes, void* stream)
+                         int out_dtype, void* workspace, size_t workspace_bytes, void* stream)
 {
-    return gemm_entry(q, x_scale, w, w_scale, bias, y, nullptr, M, N, K, scalar_scales, workspace, workspace_bytes,
-                      stream, "int8_gemm_dequant");
+    return gemm_entry(q, x_scale, w, w_scale, bias, y, nullptr, M, N, K, scalar_scales, out_dtype, workspace,
+                      workspace_bytes, stream, "int8_gemm_dequant");
 }
 
 int ck_int8_gemm_s32(const int8_t* q, const int8_t* w, int32_t* acc, int64_t M, int64_t N, int64_t K,
                      void* workspace, size_t workspace_bytes, void* stream)
 {
-    return gemm_entry(q, nullptr, w, nullptr, nullptr, nullptr, acc, M, N, K, 0, workspace, workspace_bytes, stream,
-                      "int8_gemm_s32");
+    return gemm_entry(q, nullptr, w, nullptr, nullptr, nullptr, acc, M, N, K, 0, CK_OUT_BF16, workspace,
+                      workspace_bytes, stream, "int8_gemm_s32");
 }
 
 int ck_profile_begin(int with_events)

@@ -43,7 +43,8 @@ struct GemmProblem {
     const float* w_scale = nullptr;
     const void* bias = nullptr;  // bf16 [N] or nullptr
     int scalar_scales = 0;
-    void* y = nullptr;           // bf16 [M,N]
+    void* y = nullptr;           // [M,N] of the output type
+    int out_dtype = 0;           // 0 bf16, 1 fp16, 2 fp32
     int32_t* acc = nullptr;      // int32 [M,N]
 };
 

@@ -45,6 +45,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
@@ -67,8 +68,8 @@ constexpr int THREADS = 32 * (2 + EPI_WARPS);
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr int B_BOX_ROWS = BN / 2;                       // most weight rows per TMA box
 constexpr uint32_t B_BOX_BYTES = B_BOX_ROWS * BK * 2;
-constexpr int OUT_COLS = 32;                             // columns per TMA store box
-constexpr uint32_t OUT_BUF_BYTES = 32 * OUT_COLS * 2;    // 32 rows x 64 bytes
+constexpr uint32_t OUT_ROW_BYTES = 64;                   // a TMA store box is 32 rows x 64 bytes
+constexpr uint32_t OUT_BUF_BYTES = 32 * OUT_ROW_BYTES;
 constexpr uint32_t OUT_BYTES = EPI_WARPS * 2 * OUT_BUF_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t BAR_BYTES = 256;
@@ -131,15 +132,32 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsig
     }
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+// Output element types of the epilogue (the pages' int8_linear(..., out_dtype)).
+enum : int { kOutBf16 = 0, kOutF16 = 1, kOutF32 = 2 };
+
+template <int OUT>
+struct OutType {
+    static constexpr int BYTES = OUT == kOutF32 ? 4 : 2;
+    static constexpr int BOX_COLS = (int)OUT_ROW_BYTES / BYTES;  // 32 (16-bit types) or 16 (fp32)
+    static constexpr int PER_CHUNK = 16 / BYTES;                   // values per 16-byte chunk
+};
+
+// Round two fp32 values to the output type and pack them (lower column first).
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
+    if (OUT == kOutF16) {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
 }
 
 // 10 warps put three warps on two of the four SM sub-partitions, whose register files
 // hold 16K registers each: at most 168 registers per thread.
-template <bool RAW, bool PAIR>
+template <bool RAW, bool PAIR, int OUT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const Args args)
@@ -393,65 +411,83 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             } else {
+                using OT = OutType<OUT>;
+                constexpr int PC = OT::PER_CHUNK;
                 const bool row_ok = row < args.M;
                 const float xsv = args.scalar_scales ? args.xs[0] : (row_ok ? args.xs[row] : 0.0f);
                 const int64_t row0 = m0 + quarter * 32;
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const int64_t col0 = cbase + g * OUT_COLS;
-                    if (g * OUT_COLS >= ncols || col0 >= args.N || row0 >= args.M)
+                for (int g = 0; g < 128 / OT::BOX_COLS; ++g) {
+                    const int64_t col0 = cbase + g * OT::BOX_COLS;
+                    if (g * OT::BOX_COLS >= ncols || col0 >= args.N || row0 >= args.M)
                         break;  // warp-uniform: nothing of this box is inside the tile and y
                     uint8_t* buf = obuf + (nstore & 1u) * OUT_BUF_BYTES;
                     if (lane == 0)
                         bulk_wait_group_read<1>();  // the store that last used `buf` has read it
                     __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {  // 8 columns = one 16-byte chunk of the row
-                        const int64_t col = col0 + c * 8;
-                        float wsv[8], bv[8];
-                        if (col < args.N) {
+                    for (int c = 0; c < 4; ++c) {  // one 16-byte chunk of the row: PC columns
+                        const int64_t col = col0 + c * PC;
+                        const int j0 = g * OT::BOX_COLS + c * PC;  // first running sum of the chunk
+                        float wsv[PC], bv[PC];
+                        if (col < args.N) {  // N % 8 == 0: a chunk is all in or all out
                             if (args.scalar_scales) {
 #pragma unroll
-                                for (int i = 0; i < 8; ++i)
+                                for (int i = 0; i < PC; ++i)
                                     wsv[i] = args.ws[0];
                             } else {
-                                const float4 w0 = *reinterpret_cast<const float4*>(args.ws + col);
-                                const float4 w1 = *reinterpret_cast<const float4*>(args.ws + col + 4);
-                                wsv[0] = w0.x; wsv[1] = w0.y; wsv[2] = w0.z; wsv[3] = w0.w;
-                                wsv[4] = w1.x; wsv[5] = w1.y; wsv[6] = w1.z; wsv[7] = w1.w;
-                            }
-                            if (args.bias) {
-                                const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + col);
-                                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&braw);
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    bv[2 * i] = __low2float(b2[i]);
-                                    bv[2 * i + 1] = __high2float(b2[i]);
+                                for (int i = 0; i < PC; i += 4) {
+                                    const float4 w4 = *reinterpret_cast<const float4*>(args.ws + col + i);
+                                    wsv[i] = w4.x; wsv[i + 1] = w4.y; wsv[i + 2] = w4.z; wsv[i + 3] = w4.w;
                                 }
                             }
-                        } else {
+                            if (args.bias) {
+                                if (PC == 8) {
+                                    const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + col);
+                                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&braw);
 #pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                wsv[i] = 0.0f;
+                                    for (int i = 0; i < PC / 2; ++i) {
+                                        bv[2 * i] = __low2float(b2[i]);
+                                        bv[2 * i + 1] = __high2float(b2[i]);
+                                    }
+                                } else {
+                                    const uint2 braw = *reinterpret_cast<const uint2*>(args.bias + col);
+                                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&braw);
+#pragma unroll
+                                    for (int i = 0; i < PC / 2; ++i) {
+                                        bv[2 * i] = __low2float(b2[i]);
+                                        bv[2 * i + 1] = __high2float(b2[i]);
+                                    }
+                                }
+                            }
+                        } else {  // past the last column: computed, then clipped by the store
+#pragma unroll
+                            for (int i = 0; i < PC; ++i)
+                                wsv[i] = bv[i] = 0.0f;
+                        }
+                        float t[PC];
+#pragma unroll
+                        for (int i = 0; i < PC; ++i) {
+                            t[i] = __int2float_rn(run[j0 + i]);
+                            t[i] = __fmul_rn(t[i], xsv);
+                            t[i] = __fmul_rn(t[i], wsv[i]);
+                            if (args.bias)
+                                t[i] = __fadd_rn(t[i], bv[i]);
                         }
                         uint32_t packed[4];
+                        if (OUT == kOutF32) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            float t0 = __int2float_rn(run[g * 32 + c * 8 + 2 * i]);
-                            float t1 = __int2float_rn(run[g * 32 + c * 8 + 2 * i + 1]);
-                            t0 = __fmul_rn(t0, xsv);
-                            t1 = __fmul_rn(t1, xsv);
-                            t0 = __fmul_rn(t0, wsv[2 * i]);
-                            t1 = __fmul_rn(t1, wsv[2 * i + 1]);
-                            if (args.bias) {
-                                t0 = __fadd_rn(t0, bv[2 * i]);
-                                t1 = __fadd_rn(t1, bv[2 * i + 1]);
-                            }
-                            packed[i] = pack_bf16x2(t0, t1);
+                            for (int i = 0; i < 4; ++i)
+                                packed[i] = __float_as_uint(t[i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                packed[i] = pack2<OUT>(t[2 * i], t[2 * i + 1]);
                         }
                         // 64-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ ((r >> 1) & 3)
                         const uint32_t phys = (uint32_t)c ^ (((uint32_t)lane >> 1) & 3u);
-                        *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) =
+                        *reinterpret_cast<uint4*>(buf + lane * OUT_ROW_BYTES + phys * 16) =
                             make_uint4(packed[0], packed[1], packed[2], packed[3]);
                     }
                     fence_proxy_async_smem();
@@ -546,7 +582,7 @@ static bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ba
     return true;
 }
 
-template <bool RAW, bool PAIR>
+template <bool RAW, bool PAIR, int OUT>
 static cudaError_t ensure_smem_attr(int device)
 {
     static bool done[64] = {};
@@ -554,7 +590,8 @@ static cudaError_t ensure_smem_attr(int device)
     std::lock_guard<std::mutex> lock(mu);
     if (device >= 0 && device < 64 && done[device])
         return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR, OUT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)gemm::Mode<PAIR>::SMEM_BYTES);
     if (e == cudaSuccess && device >= 0 && device < 64)
         done[device] = true;
@@ -592,15 +629,13 @@ static cudaError_t resident_units(const DeviceInfo& dev, int64_t* out)
     std::lock_guard<std::mutex> lock(mu);
     int& n = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
     if (n == 0) {
-        cudaError_t e = ensure_smem_attr<false, true>(dev.device);
-        if (e == cudaSuccess)
-            e = ensure_smem_attr<true, true>(dev.device);
+        cudaError_t e = ensure_smem_attr<false, true, gemm::kOutBf16>(dev.device);
         if (e != cudaSuccess)
             return e;
         cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = make_config(true, gemm::Mode<true>::SMEM_BYTES, nullptr, attr);
         cfg.gridDim = dim3(2 * (dev.sm_count / 2));
-        e = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_kernel<false, true>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_kernel<false, true, gemm::kOutBf16>, &cfg);
         if (e != cudaSuccess)
             return e;
         if (n <= 0)
@@ -637,12 +672,12 @@ static int choose_tile_width(int64_t N, int64_t units_m, int64_t resident)
 
 // Launch with programmatic stream serialization and, for pairs, 2-CTA clusters; the
 // persistent grid is as many units as can be resident at once.
-template <bool RAW, bool PAIR>
+template <bool RAW, bool PAIR, int OUT>
 static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                                  const gemm::Args& a, const DeviceInfo& dev, cudaStream_t s)
 {
     using namespace gemm;
-    cudaError_t e = ensure_smem_attr<RAW, PAIR>(dev.device);
+    cudaError_t e = ensure_smem_attr<RAW, PAIR, OUT>(dev.device);
     if (e != cudaSuccess)
         return e;
     int64_t resident = 0;
@@ -652,7 +687,7 @@ static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB,
     cudaLaunchConfig_t cfg = make_config(PAIR, Mode<PAIR>::SMEM_BYTES, s, attr);
     const int64_t units = std::min<int64_t>(a.num_units, resident);
     cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units));
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR>, tmA, tmB, tmY, a);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR, OUT>, tmA, tmB, tmY, a);
 }
 
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why)
@@ -663,11 +698,21 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, p.K, p.M, (uint64_t)p.K * 2, BK, BM,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
         return cudaErrorInvalidValue;
+    if (!raw && p.out_dtype != kOutBf16 && p.out_dtype != kOutF16 && p.out_dtype != kOutF32) {
+        *why = "unknown output type";
+        return cudaErrorInvalidValue;
+    }
     if (raw) {
         tmY = tmA;  // unused by the raw-accumulator kernel
-    } else if (!make_map_2d(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.y, p.N, p.M, (uint64_t)p.N * 2, OUT_COLS, 32,
-                            CU_TENSOR_MAP_SWIZZLE_64B, why)) {
-        return cudaErrorInvalidValue;
+    } else {
+        const bool f32 = p.out_dtype == kOutF32;
+        const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                           : (p.out_dtype == kOutF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+        const uint32_t esize = f32 ? 4u : 2u;
+        if (!make_map_2d(&tmY, dt, p.y, p.N, p.M, (uint64_t)p.N * esize, OUT_ROW_BYTES / esize, 32,
+                         CU_TENSOR_MAP_SWIZZLE_64B, why))
+            return cudaErrorInvalidValue;
     }
     Args a;
     a.M = p.M;
@@ -700,10 +745,19 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
         return cudaErrorInvalidValue;
     if (raw)
-        return pair ? launch_kernel<true, true>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<true, false>(tmA, tmB, tmY, a, dev, s);
-    return pair ? launch_kernel<false, true>(tmA, tmB, tmY, a, dev, s)
-                : launch_kernel<false, false>(tmA, tmB, tmY, a, dev, s);
+        return pair ? launch_kernel<true, true, kOutBf16>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<true, false, kOutBf16>(tmA, tmB, tmY, a, dev, s);
+    switch (p.out_dtype) {
+    case kOutF16:
+        return pair ? launch_kernel<false, true, kOutF16>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutF16>(tmA, tmB, tmY, a, dev, s);
+    case kOutF32:
+        return pair ? launch_kernel<false, true, kOutF32>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutF32>(tmA, tmB, tmY, a, dev, s);
+    default:
+        return pair ? launch_kernel<false, true, kOutBf16>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutBf16>(tmA, tmB, tmY, a, dev, s);
+    }
 }
 
 cudaError_t read_device_error(unsigned int* value, bool clear)

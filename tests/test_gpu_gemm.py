@@ -8,7 +8,7 @@ import torch
 import oracle
 import int8_weight_quantized_gb300 as ck
 from int8_weight_quantized_gb300 import synthetic
-from helpers import bits, bf16_ulp_distance, MAX_ULP
+from helpers import bits, bf16_ulp_distance, out_bits, ulp_distance, MAX_ULP
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -95,3 +95,66 @@ def test_s32_every_tile_width(monkeypatch, bn, pair):
     q = synthetic.int8_uniform((M, K), seed=bn + 1)
     w = synthetic.int8_uniform((N, K), seed=bn + 2)
     assert np.array_equal(gpu_acc(q, w), oracle.gemm_s32(q.numpy(), w.numpy()))
+
+
+TYPED = [(torch.float16, oracle.OUT_F16), (torch.float32, oracle.OUT_F32), (torch.bfloat16, oracle.OUT_BF16)]
+
+
+def typed_reference(q, w, xs, ws, b, scalar, code):
+    acc = oracle.gemm_s32(q.numpy(), w.numpy())
+    ref = oracle.dequant_typed(acc, xs.numpy(), ws.numpy(), None if b is None else bits(b), scalar_scales=scalar,
+                               out_dtype=code)
+    return ref.view(np.uint32) if code == oracle.OUT_F32 else ref
+
+
+@pytest.mark.parametrize("out_dtype,code", TYPED)
+@pytest.mark.parametrize("scalar,with_bias", [(False, True), (True, False), (False, False)])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (129, 264, 1040), (1, 8, 16), (385, 520, 192)])
+def test_dequant_output_types(M, N, K, scalar, with_bias, out_dtype, code):
+    """The epilogue's fp32 value rounded to fp16 / stored as fp32 (the out_dtype of
+    int8_linear): within 1 ulp of the oracle in that type."""
+    q = synthetic.int8_uniform((M, K), seed=21 + M)
+    w = synthetic.int8_uniform((N, K), seed=22 + N)
+    xs = synthetic.scale_uniform(1 if scalar else M, seed=23, mul=0.02)
+    ws = synthetic.scale_uniform(1 if scalar else N, seed=24, mul=0.01)
+    b = synthetic.normal_bf16((1, N), seed=25, std=0.5).reshape(N) if with_bias else None
+    ref = typed_reference(q, w, xs, ws, b, scalar, code)
+    y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), None if b is None else b.to(DEV),
+                                scalar_scales=scalar, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert y.dtype == out_dtype
+    d = ulp_distance(out_bits(y), ref)
+    assert d.max() <= MAX_ULP, "max ulp %d at %s" % (d.max(), np.unravel_index(d.argmax(), d.shape))
+
+
+def test_f16_output_overflow_and_subnormals():
+    """Scales that push outputs past fp16's range (-> +-inf) and into its subnormals."""
+    M, N, K = 130, 264, 256
+    q = synthetic.int8_uniform((M, K), seed=31)
+    w = synthetic.int8_uniform((N, K), seed=32)
+    xs = synthetic.scale_uniform(M, seed=33, mul=1.0)
+    xs[::3] *= 1e-9   # |y| ~ 1e-9 * 1e4 * ws: fp16 subnormals
+    xs[1::3] *= 1e3   # |y| beyond 65504
+    ws = synthetic.scale_uniform(N, seed=34, mul=0.01)
+    ref = typed_reference(q, w, xs, ws, None, False, oracle.OUT_F16)
+    y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), None, out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    got = out_bits(y)
+    assert np.any((ref & 0x7FFF) == 0x7C00) and np.any(((ref & 0x7C00) == 0) & ((ref & 0x3FF) != 0))
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("bn", [256, 160, 96, 32])
+def test_f32_output_every_tile_width(monkeypatch, bn):
+    """fp32 outputs leave the tile in 16-column boxes: every tile width, ragged M and N."""
+    monkeypatch.setenv("CK_GEMM_BN", str(bn))
+    M, N, K = 300, 712, 272
+    q = synthetic.int8_uniform((M, K), seed=bn + 41)
+    w = synthetic.int8_uniform((N, K), seed=bn + 42)
+    xs = synthetic.scale_uniform(M, seed=43, mul=0.02)
+    ws = synthetic.scale_uniform(N, seed=44, mul=0.01)
+    b = synthetic.normal_bf16((1, N), seed=45, std=0.5).reshape(N)
+    ref = typed_reference(q, w, xs, ws, b, False, oracle.OUT_F32)
+    y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert ulp_distance(out_bits(y), ref).max() <= MAX_ULP

@@ -9,7 +9,7 @@ import torch
 import oracle
 import int8_weight_quantized_gb300 as ck
 from int8_weight_quantized_gb300 import synthetic
-from helpers import bits, bf16_ulp_distance, MAX_ULP
+from helpers import bits, bf16_ulp_distance, out_bits, ulp_distance, MAX_ULP
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -37,6 +37,29 @@ def run_full(spec):
 
 def test_per_row_256x512x512():
     run_full(synthetic.PER_ROW_SMALL)
+
+
+@pytest.mark.parametrize("out_dtype,code", [(torch.float16, oracle.OUT_F16), (torch.float32, oracle.OUT_F32)])
+@pytest.mark.parametrize("mode", [synthetic.TENSORWISE, synthetic.PER_ROW, synthetic.CONVROT])
+def test_output_types(mode, out_dtype, code):
+    """int8_linear(x, w, ws, out_dtype): the same layer with fp16 and fp32 outputs."""
+    M, N, K = 300, 264, 1152
+    x = synthetic.normal_bf16((M, K), seed=61 + mode)
+    if mode == synthetic.CONVROT:
+        w, ws = oracle.prepare_convrot_weight(synthetic.normal_f32((N, K), seed=62, std=0.02).numpy())
+        w, ws = torch.from_numpy(w), torch.from_numpy(ws)
+    else:
+        w = synthetic.int8_uniform((N, K), seed=62)
+        ws = synthetic.scale_uniform(1 if mode == synthetic.TENSORWISE else N, seed=63)
+    b = synthetic.normal_bf16((1, N), seed=64, std=0.5).reshape(N)
+    ref = oracle.int8_linear(bits(x), w.numpy(), ws.numpy(), bits(b), mode=mode, out_dtype=code)["y"]
+    if code == oracle.OUT_F32:
+        ref = ref.view(np.uint32)
+    y = ck.ck_int8_linear(x.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), mode=mode, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert y.dtype == out_dtype
+    d = ulp_distance(out_bits(y), ref)
+    assert d.max() <= MAX_ULP, "max ulp %d at %s" % (d.max(), np.unravel_index(d.argmax(), d.shape))
 
 
 def test_tensorwise_4096_cubed_with_bias():

@@ -52,10 +52,10 @@ def _call_linear(lib, M, N, K, mode, **kw):
     import ctypes
     P = ctypes.c_void_p
     ptr = P(4096)  # never dereferenced: validation fails first
-    args = dict(x=ptr, w=ptr, ws=ptr, bias=None, y=ptr, work=ptr, nbytes=1 << 40)
+    args = dict(x=ptr, w=ptr, ws=ptr, bias=None, y=ptr, work=ptr, nbytes=1 << 40, out_dtype=0)
     args.update(kw)
     return lib.ck_int8_linear(args["x"], args["w"], args["ws"], args["bias"], args["y"], M, N, K, mode,
-                              args["work"], args["nbytes"], None)
+                              args["out_dtype"], args["work"], args["nbytes"], None)
 
 
 @pytest.mark.parametrize("M,N,K,mode,what", [
@@ -72,6 +72,19 @@ def test_invalid_shapes_are_rejected_without_a_gpu(lib, M, N, K, mode, what):
     st = _call_linear(lib, M, N, K, mode)
     assert st == ck.CK_ERR_INVALID_ARG
     assert what in ck.ck_last_error()
+
+
+def test_unknown_output_type_is_rejected(lib):
+    import int8_weight_quantized_gb300 as ck
+    assert _call_linear(lib, 16, 16, 32, 1, out_dtype=3) == ck.CK_ERR_INVALID_ARG
+    assert "out_dtype" in ck.ck_last_error()
+    import ctypes
+    P = ctypes.c_void_p(4096)
+    st = lib.ck_int8_gemm_dequant(P, P, P, P, None, P, 16, 16, 32, 0, -1, P, 1 << 40, None)
+    assert st == ck.CK_ERR_INVALID_ARG and "out_dtype" in ck.ck_last_error()
+    with pytest.raises(ValueError):
+        ck.ck_int8_linear(torch.zeros((16, 32), dtype=torch.bfloat16), torch.zeros((16, 32), dtype=torch.int8),
+                          torch.ones(16), out_dtype=torch.int32)
 
 
 def test_null_and_misaligned_pointers_are_rejected(lib):
