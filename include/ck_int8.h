@@ -168,6 +168,16 @@ int ck_int8_gemm_s32(const int8_t *q, const int8_t *w, int32_t *acc, int64_t M, 
 int ck_profile_begin(int with_events);
 int ck_profile_end(double *ms, int64_t *launches, int nkinds);
 
+/* The GEMM launch configuration ck_int8_linear / ck_int8_gemm_* would use for an
+ * M x N x K problem on the current device (the tile choice of issue #280, "Kernel used",
+ * made per launch here): *bn = tile width in output columns (a multiple of 32, at most
+ * 256), *cta_pair = 1 if two CTAs share a 256-row tile (tcgen05 cta_group::2) else 0
+ * (128-row tiles), *resident_units = how many pairs / CTAs run at once (may be NULL).
+ * The environment variables CK_GEMM_BN=<width> and CK_GEMM_PAIR=0 / 1 (single CTAs /
+ * pairs only) override the choice for A/B timing; the query reports the result.  Host memory outputs; no work
+ * is enqueued. */
+int ck_gemm_tile_config(int64_t M, int64_t N, int64_t K, int *bn, int *cta_pair, int64_t *resident_units);
+
 /* Text of the last non-OK status returned on this host thread ("" if none). */
 const char *ck_last_error(void);
 

@@ -2,6 +2,7 @@
 // device check, workspace layout, and the launch sequence of each entry point.
 // Every entry point validates before it enqueues anything and never synchronises the
 // host (except the two diagnostics at the end).
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -523,6 +524,27 @@ int ck_profile_end(double* ms, int64_t* launches, int nkinds)
     }
     g_prof_recs.clear();
     return status;
+}
+
+int ck_gemm_tile_config(int64_t M, int64_t N, int64_t K, int* bn, int* cta_pair, int64_t* resident_units)
+{
+    int st = check_gemm_shape(M, N, K);
+    if (st != CK_OK)
+        return st;
+    CK_REQUIRE_PTR(bn);
+    CK_REQUIRE_PTR(cta_pair);
+    DeviceInfo dev;
+    if ((st = check_device(&dev)) != CK_OK)
+        return st;
+    GemmPlan plan;
+    cudaError_t e = plan_gemm(std::max<int64_t>(M, 1), N, dev, &plan);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "GEMM planning");
+    *bn = plan.bn;
+    *cta_pair = plan.pair ? 1 : 0;
+    if (resident_units)
+        *resident_units = plan.resident;
+    return CK_OK;
 }
 
 int ck_device_error(int clear)

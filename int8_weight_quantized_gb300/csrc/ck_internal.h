@@ -59,6 +59,14 @@ cudaError_t current_device(DeviceInfo* info);
 
 // Kernel launchers.  Each returns cudaSuccess or the launch error; `why` gets a
 // description of a failure that is not a CUDA error.
+// The GEMM launch configuration for an M x N output: CTA pairs or single CTAs, the tile
+// width (a multiple of 32 up to 256) and how many units can be resident at once.
+struct GemmPlan {
+    bool pair = false;
+    int bn = 0;
+    int64_t resident = 0;
+};
+cudaError_t plan_gemm(int64_t M, int64_t N, const DeviceInfo& dev, GemmPlan* plan);
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why);
 cudaError_t launch_quantize_rows(const void* x, int64_t M, int64_t K, bool rotate, int8_t* q8, void* q16,
                                  float* x_scale, const DeviceInfo& dev, cudaStream_t s);

@@ -645,29 +645,46 @@ static cudaError_t resident_units(const DeviceInfo& dev, int64_t* out)
     return cudaSuccess;
 }
 
-// The tile width (a multiple of 32 up to 256) that finishes soonest: `units_m` rows of
-// units times ceil(N / bn) columns run in ceil(units / resident) waves, and a wave costs
-// about bn + 64 column-equivalents (the activation tile costs as much as 64 weight rows
-// to stage).  CK_GEMM_BN=<width> forces a width (A/B timing of the same work).
-static int choose_tile_width(int64_t N, int64_t units_m, int64_t resident)
+// Time of one 64-deep k-block of one unit, in units of 0.01 ns, as measured on GB300
+// over tile widths 32..256 (25900x16384x4096, many waves): a CTA pair's 256-row unit
+// takes about 305 + 0.15 * bn ns, a single CTA's 128-row unit about 300 + 0.29 * bn ns.
+// Narrow tiles hardly save time per k-block (the MMA chain has a latency floor near the
+// 256-wide tile's throughput time), so the width mainly trades wave quantization.
+static int64_t kblock_cost(bool pair, int bn)
 {
+    return pair ? 30500 + 15 * (int64_t)bn : 30000 + 29 * (int64_t)bn;
+}
+
+// The configuration that finishes soonest: `units` = rows of units times ceil(N / bn)
+// columns run in ceil(units / resident) waves of kblock_cost() each.
+// CK_GEMM_BN=<width> forces a width (A/B timing).
+static void choose_tile(int64_t N, int64_t tiles_m, int64_t resident_pair, int64_t resident_single,
+                        bool pair_allowed, bool single_allowed, GemmPlan* plan)
+{
+    int force_bn = 0;
     if (const char* force = std::getenv("CK_GEMM_BN")) {
         const int f = std::atoi(force);
         if (f >= 32 && f <= gemm::BN && f % 32 == 0)
-            return f;
+            force_bn = f;
     }
-    int best = gemm::BN;
     int64_t best_cost = -1;
-    for (int bn = gemm::BN; bn >= 128; bn -= 32) {
-        const int64_t units = units_m * ((N + bn - 1) / bn);
-        const int64_t waves = (units + resident - 1) / resident;
-        const int64_t cost = waves * (bn + 64);
-        if (best_cost < 0 || cost < best_cost) {
-            best = bn;
-            best_cost = cost;
+    for (int p = pair_allowed ? 1 : 0; p >= (single_allowed ? 0 : 1); --p) {
+        const int64_t units_m = p ? (tiles_m + 1) / 2 : tiles_m;
+        const int64_t resident = p ? resident_pair : resident_single;
+        for (int bn = gemm::BN; bn >= 32; bn -= 32) {
+            if (force_bn && bn != force_bn)
+                continue;
+            const int64_t units = units_m * ((N + bn - 1) / bn);
+            const int64_t waves = (units + resident - 1) / resident;
+            const int64_t cost = waves * kblock_cost(p != 0, bn);
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost;
+                plan->pair = p != 0;
+                plan->bn = bn;
+                plan->resident = resident;
+            }
         }
     }
-    return best;
 }
 
 // Launch with programmatic stream serialization and, for pairs, 2-CTA clusters; the
@@ -688,6 +705,24 @@ static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB,
     const int64_t units = std::min<int64_t>(a.num_units, resident);
     cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units));
     return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR, OUT>, tmA, tmB, tmY, a);
+}
+
+cudaError_t plan_gemm(int64_t M, int64_t N, const DeviceInfo& dev, GemmPlan* plan)
+{
+    const int64_t tiles_m = (M + gemm::BM - 1) / gemm::BM;
+    // CK_GEMM_PAIR=0 / =1 restricts the choice to single CTAs / CTA pairs (A/B timing);
+    // a problem with one 128-row tile row always runs single CTAs
+    const char* force = std::getenv("CK_GEMM_PAIR");
+    const bool pair_allowed = tiles_m >= 2 && !(force && std::strcmp(force, "0") == 0);
+    const bool single_allowed = !(pair_allowed && force && std::strcmp(force, "1") == 0);
+    int64_t resident_pair = 0, resident_single = 0;
+    cudaError_t e = resident_units<false>(dev, &resident_single);
+    if (e == cudaSuccess && pair_allowed)
+        e = resident_units<true>(dev, &resident_pair);
+    if (e != cudaSuccess)
+        return e;
+    choose_tile(N, tiles_m, resident_pair, resident_single, pair_allowed, single_allowed, plan);
+    return cudaSuccess;
 }
 
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why)
@@ -726,17 +761,15 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.num_kb = (int)((p.K + BK - 1) / BK);
     a.scalar_scales = p.scalar_scales;
     a.timeout_ns = DEFAULT_TIMEOUT_NS;
-    // CK_GEMM_PAIR=0 forces one CTA per 128-row tile (A/B timing of the same work)
-    const char* force = std::getenv("CK_GEMM_PAIR");
-    const bool pair = a.tiles_m >= 2 && !(force && std::strcmp(force, "0") == 0);
+    GemmPlan plan;
+    const cudaError_t e = plan_gemm(p.M, p.N, dev, &plan);
+    if (e != cudaSuccess)
+        return e;
+    const bool pair = plan.pair;
     a.unit_rows = pair ? 2 : 1;
     a.units_m = (a.tiles_m + a.unit_rows - 1) / a.unit_rows;
     a.group_m = pair ? 4 : 8;  // 8 tile rows per sweep either way
-    int64_t resident = 0;
-    const cudaError_t e = pair ? resident_units<true>(dev, &resident) : resident_units<false>(dev, &resident);
-    if (e != cudaSuccess)
-        return e;
-    a.bn = choose_tile_width(p.N, a.units_m, resident);
+    a.bn = plan.bn;
     a.tiles_n = (int)((p.N + a.bn - 1) / a.bn);
     a.num_units = (int64_t)a.units_m * a.tiles_n;
     a.idesc = (pair ? Mode<true>::IDESC_M : Mode<false>::IDESC_M) | ((uint32_t)(a.bn >> 3) << 17);

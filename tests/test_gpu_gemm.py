@@ -91,6 +91,7 @@ def test_s32_every_tile_width(monkeypatch, bn, pair):
     CTA pairs and with single CTAs, gives the exact accumulators (ragged M, N and K)."""
     monkeypatch.setenv("CK_GEMM_BN", str(bn))
     monkeypatch.setenv("CK_GEMM_PAIR", pair)
+    assert ck.ck_gemm_tile_config(300, 712, 1104)[:2] == (bn, pair == "1")
     M, N, K = 300, 712, 1104
     q = synthetic.int8_uniform((M, K), seed=bn + 1)
     w = synthetic.int8_uniform((N, K), seed=bn + 2)
@@ -158,3 +159,18 @@ def test_f32_output_every_tile_width(monkeypatch, bn):
     y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert ulp_distance(out_bits(y), ref).max() <= MAX_ULP
+
+
+def test_tile_config_query(monkeypatch):
+    """The planner's choice is a valid configuration, follows the A/B overrides, and the
+    GEMM stays exact when launched with whatever it picked."""
+    for M, N, K in [(4096, 4096, 4096), (128, 4096, 4096), (80666, 28672, 5376), (1, 8, 16)]:
+        bn, pair, resident = ck.ck_gemm_tile_config(M, N, K)
+        assert bn % 32 == 0 and 32 <= bn <= 256 and resident >= 1
+        assert not pair or (M + 127) // 128 >= 2
+    monkeypatch.setenv("CK_GEMM_BN", "96")
+    monkeypatch.setenv("CK_GEMM_PAIR", "0")
+    assert ck.ck_gemm_tile_config(4096, 4096, 4096)[:2] == (96, False)
+    monkeypatch.setenv("CK_GEMM_PAIR", "1")
+    assert ck.ck_gemm_tile_config(4096, 4096, 4096)[:2] == (96, True)
+    assert ck.ck_gemm_tile_config(128, 4096, 4096)[:2] == (96, False)  # one tile row: no pair

@@ -123,3 +123,13 @@ def test_product_package_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "ck_oracle" not in text, f
+
+
+def test_tile_config_query_validates_without_a_gpu(lib):
+    import ctypes
+    import int8_weight_quantized_gb300 as ck
+    bn, pair = ctypes.c_int(), ctypes.c_int()
+    assert lib.ck_gemm_tile_config(16, 12, 32, ctypes.byref(bn), ctypes.byref(pair), None) == ck.CK_ERR_INVALID_ARG
+    st = lib.ck_gemm_tile_config(16, 16, 32, ctypes.byref(bn), ctypes.byref(pair), None)
+    if not torch.cuda.is_available():
+        assert st in (ck.CK_ERR_CUDA, ck.CK_ERR_UNSUPPORTED_DEVICE)
