@@ -570,27 +570,34 @@ __global__ void __launch_bounds__(256) quant_flat_kernel(const uint4* __restrict
 // (re-read from L2) into bf16 codes.
 // Hand-off without atomics or resets: block b writes its maximum into slot b of the
 // caller's workspace and then, with release semantics, this launch's 64-bit epoch next
-// to it; block 0 waits until every slot carries the epoch, reduces the maxima and
-// publishes the result the same way in a final slot, which every other block polls.
-// Values left by any earlier launch carry another epoch and are never taken.  The grid
-// never exceeds the number of co-resident blocks, so every block gets to publish; the
-// waits are bounded all the same (a timeout sets `err` and the block goes on).
+// to it; every block then polls all slots (relaxed loads, one acquire fence once every
+// slot carries the epoch) and reduces the maxima itself, so the maximum is known one
+// round trip after the last block published.  Values left by any earlier launch carry
+// another epoch and are never taken.  The grid never exceeds the number of co-resident
+// blocks (nor kMaxSlotsPerThread * 256), so every block gets to publish; the waits are
+// bounded all the same (a timeout sets `err` and the block goes on).
 struct alignas(16) EpochSlot {
     unsigned long long epoch;
     float value;
     float pad;
 };
+constexpr int kMaxSlotsPerThread = 4;  // slots one of the 256 threads watches
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p)
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p)
 {
     unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
 __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v)
 {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu()
+{
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
@@ -601,10 +608,8 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
     griddep_wait();
     griddep_launch_dependents();
     __shared__ float red[8];
-    __shared__ float s_amax;
-    __shared__ int s_timeout;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    EpochSlot* done = slots + gridDim.x;
+    const int G = (int)gridDim.x;
     // 1. this block's maximum, published
     __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec; base += UNROLL * stride) {
@@ -621,8 +626,6 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
     float m = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
     if ((threadIdx.x & 31) == 0)
         red[threadIdx.x >> 5] = m;
-    if (threadIdx.x == 0)
-        s_timeout = 0;
     __syncthreads();
     if (threadIdx.x == 0) {
         float bm = 0.0f;
@@ -633,48 +636,44 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
     }
     // 2. the weight widening hides the wait for the slowest block
     widen_share(w8, w_n16, w16);
-    // 3. the global maximum
-    if (blockIdx.x == 0) {
-        const uint64_t t0 = globaltimer_ns();
-        m = 0.0f;
-        for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) {
-            uint32_t polls = 0;
-            while (ld_acquire_u64(&slots[i].epoch) != epoch) {
-                if ((++polls & 31u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
-                    s_timeout = 1;
-                    break;
-                }
-            }
-            m = fmaxf(m, __ldcg(&slots[i].value));
-        }
-        m = warp_max(m);
-        if ((threadIdx.x & 31) == 0)
-            red[threadIdx.x >> 5] = m;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float g = 0.0f;
-            for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
-                g = fmaxf(g, red[i]);
-            s_amax = g;
-            done->value = g;
-            st_release_u64(&done->epoch, epoch);
-            if (s_timeout)
+    // 3. the global maximum: every slot carries this launch's epoch
+    uint32_t seen = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxSlotsPerThread; ++j)
+        if ((int)threadIdx.x + 256 * j >= G)
+            seen |= 1u << j;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t round = 1;; ++round) {
+#pragma unroll
+        for (int j = 0; j < kMaxSlotsPerThread; ++j)
+            if (!(seen & (1u << j)) && ld_relaxed_u64(&slots[threadIdx.x + 256 * j].epoch) == epoch)
+                seen |= 1u << j;
+        int give_up = 0;
+        if ((round & 15u) == 0 && threadIdx.x == 0 && globaltimer_ns() - t0 > timeout_ns)
+            give_up = 1;
+        if (__syncthreads_or(give_up)) {
+            if (threadIdx.x == 0)
                 atomicOr(err, kErrWaitGrid);
+            break;
         }
-    } else if (threadIdx.x == 0) {
-        const uint64_t t0 = globaltimer_ns();
-        uint32_t polls = 0;
-        while (ld_acquire_u64(&done->epoch) != epoch) {
-            __nanosleep(200);
-            if ((++polls & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
-                atomicOr(err, kErrWaitGrid);
-                break;
-            }
-        }
-        s_amax = __ldcg(&done->value);
+        if (__syncthreads_and(seen == (1u << kMaxSlotsPerThread) - 1u))
+            break;
     }
+    fence_acq_rel_gpu();  // with the relaxed epoch loads: acquire of every block's release
+    m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxSlotsPerThread; ++j)
+        if ((int)threadIdx.x + 256 * j < G)
+            m = fmaxf(m, __ldcg(&slots[threadIdx.x + 256 * j].value));
+    m = warp_max(m);
+    __syncthreads();  // every warp is done with red[] from step 1
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = m;
     __syncthreads();
-    const float sc = __fdiv_rn(s_amax, 127.0f);
+    float g = 0.0f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
+        g = fmaxf(g, red[i]);
+    const float sc = __fdiv_rn(g, 127.0f);
     if (blockIdx.x == 0 && threadIdx.x == 0)
         xs[0] = sc;
     // 4. quantize this block's slice
@@ -898,7 +897,7 @@ unsigned long long next_prep_epoch()
 
 size_t prep_tensorwise_scratch_bytes(int max_blocks)
 {
-    return sizeof(quant::EpochSlot) * (size_t)(max_blocks + 1);
+    return sizeof(quant::EpochSlot) * (size_t)max_blocks;
 }
 
 cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q16, float* x_scale, void* scratch,
@@ -907,7 +906,8 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
 {
     const int64_t nvec = (M * K) >> 3;
     const int64_t want = std::max<int64_t>(1, (nvec + 255) / 256);
-    const int grid = (int)std::min<int64_t>(std::min<int64_t>(want, prep_capacity(dev)), max_blocks);
+    const int64_t cap = std::min<int64_t>(prep_capacity(dev), (int64_t)quant::kMaxSlotsPerThread * 256);
+    const int grid = (int)std::min<int64_t>(std::min<int64_t>(want, cap), max_blocks);
     unsigned int* err = nullptr;
     cudaError_t e = device_error_ptr(&err);
     if (e != cudaSuccess)
