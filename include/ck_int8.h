@@ -172,11 +172,16 @@ int ck_profile_end(double *ms, int64_t *launches, int nkinds);
  * M x N x K problem on the current device (the tile choice of issue #280, "Kernel used",
  * made per launch here): *bn = tile width in output columns (a multiple of 32, at most
  * 256), *cta_pair = 1 if two CTAs share a 256-row tile (tcgen05 cta_group::2) else 0
- * (128-row tiles), *resident_units = how many pairs / CTAs run at once (may be NULL).
- * The environment variables CK_GEMM_BN=<width> and CK_GEMM_PAIR=0 / 1 (single CTAs /
- * pairs only) override the choice for A/B timing; the query reports the result.  Host memory outputs; no work
- * is enqueued. */
-int ck_gemm_tile_config(int64_t M, int64_t N, int64_t K, int *bn, int *cta_pair, int64_t *resident_units);
+ * (128-row tiles), *resident_units = how many pairs / CTAs run at once (may be NULL),
+ * *k_split = into how many K-slices each unit of the last partial wave is split over
+ * otherwise idle pairs / CTAs (1 = none; may be NULL).  Split slices add their exact
+ * int32 partial sums, so the result does not depend on the split.
+ * The environment variables CK_GEMM_BN=<width>, CK_GEMM_PAIR=0 / 1 (single CTAs / pairs
+ * only) and CK_GEMM_SPLIT=1 (no split) / <s> (s slices where possible) override the
+ * choice for A/B timing; the query reports the result.  Host memory outputs; no work is
+ * enqueued. */
+int ck_gemm_tile_config(int64_t M, int64_t N, int64_t K, int *bn, int *cta_pair, int64_t *resident_units,
+                        int *k_split);
 
 /* Text of the last non-OK status returned on this host thread ("" if none). */
 const char *ck_last_error(void);

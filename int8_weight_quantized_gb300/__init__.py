@@ -58,7 +58,7 @@ def load_library(path=None):
         "ck_profile_end": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I], I),
         "ck_last_error": ([], ctypes.c_char_p),
         "ck_device_error": ([I], I),
-        "ck_gemm_tile_config": ([I64, I64, I64, P, P, P], I),
+        "ck_gemm_tile_config": ([I64, I64, I64, P, P, P, P], I),
         "ck_selftest_wait_timeout": ([ctypes.c_uint64, P], I),
     }
     for name, (args, res) in sig.items():
@@ -235,10 +235,11 @@ def ck_last_error():
 
 
 def ck_gemm_tile_config(M, N, K):
-    """(bn, cta_pair, resident_units) of the GEMM launch for an M x N x K problem."""
-    bn, pair, res = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
-    _check(load_library().ck_gemm_tile_config(M, N, K, ctypes.byref(bn), ctypes.byref(pair), ctypes.byref(res)))
-    return bn.value, bool(pair.value), res.value
+    """(bn, cta_pair, resident_units, k_split) of the GEMM launch for an M x N x K problem."""
+    bn, pair, res, split = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64(), ctypes.c_int()
+    _check(load_library().ck_gemm_tile_config(M, N, K, ctypes.byref(bn), ctypes.byref(pair), ctypes.byref(res),
+                                              ctypes.byref(split)))
+    return bn.value, bool(pair.value), res.value, split.value
 
 
 def ck_device_error(clear=True):

@@ -98,13 +98,14 @@ struct LinearWorkspace {
     void* b16;        // bf16 [N,K]: weight as tensor-core operand
     float* xs;        // fp32 [M] or [1]
     void* scratch;    // tensorwise: the blocks' maxima, exchanged within one launch
+    void* tail;       // the GEMM's K-split tail: partial sums and arrival slots
 };
 
 size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int mode, int nparts)
 {
     return align_up((size_t)M * K * 2) + align_up((size_t)N * K * 2) +
            align_up(sizeof(float) * (size_t)(mode == CK_TENSORWISE ? 1 : (M > 0 ? M : 1))) +
-           align_up(prep_tensorwise_scratch_bytes(nparts));
+           align_up(prep_tensorwise_scratch_bytes(nparts)) + align_up(gemm_tail_bytes(M, N));
 }
 
 LinearWorkspace carve_linear(void* ws, int64_t M, int64_t N, int64_t K, int mode)
@@ -118,12 +119,14 @@ LinearWorkspace carve_linear(void* ws, int64_t M, int64_t N, int64_t K, int mode
     w.xs = reinterpret_cast<float*>(p);
     p += align_up(sizeof(float) * (size_t)(mode == CK_TENSORWISE ? 1 : (M > 0 ? M : 1)));
     w.scratch = p;
+    p += align_up(prep_tensorwise_scratch_bytes(kMaxPartialsForLayout));
+    w.tail = p;
     return w;
 }
 
 size_t gemm_ws_bytes(int64_t M, int64_t N, int64_t K)
 {
-    return align_up((size_t)M * K * 2) + align_up((size_t)N * K * 2);
+    return align_up((size_t)M * K * 2) + align_up((size_t)N * K * 2) + align_up(gemm_tail_bytes(M, N));
 }
 
 const int kMaxPartials = kMaxPartialsForLayout;
@@ -366,6 +369,7 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
     p.scalar_scales = mode == CK_TENSORWISE;
     p.y = y;
     p.out_dtype = out_dtype;
+    p.tail = ws.tail;
     std::string why;
     {
         ProfScope ps(kProfGemm, 1, s);
@@ -441,6 +445,7 @@ static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, co
     uint8_t* p8 = static_cast<uint8_t*>(workspace);
     void* a16 = p8;
     void* b16 = p8 + align_up((size_t)M * K * 2);
+    void* tail = static_cast<uint8_t*>(b16) + align_up((size_t)N * K * 2);
     cudaError_t e;
     {
         ProfScope ps(kProfWiden, 1, s);
@@ -461,6 +466,7 @@ static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, co
     p.y = acc ? nullptr : y;
     p.out_dtype = out_dtype;
     p.acc = acc;
+    p.tail = tail;
     std::string why;
     {
         ProfScope ps(kProfGemm, 1, s);
@@ -526,7 +532,8 @@ int ck_profile_end(double* ms, int64_t* launches, int nkinds)
     return status;
 }
 
-int ck_gemm_tile_config(int64_t M, int64_t N, int64_t K, int* bn, int* cta_pair, int64_t* resident_units)
+int ck_gemm_tile_config(int64_t M, int64_t N, int64_t K, int* bn, int* cta_pair, int64_t* resident_units,
+                        int* k_split)
 {
     int st = check_gemm_shape(M, N, K);
     if (st != CK_OK)
@@ -537,13 +544,15 @@ int ck_gemm_tile_config(int64_t M, int64_t N, int64_t K, int* bn, int* cta_pair,
     if ((st = check_device(&dev)) != CK_OK)
         return st;
     GemmPlan plan;
-    cudaError_t e = plan_gemm(std::max<int64_t>(M, 1), N, dev, &plan);
+    cudaError_t e = plan_gemm(std::max<int64_t>(M, 1), N, K, dev, &plan);
     if (e != cudaSuccess)
         return cuda_fail(e, "GEMM planning");
     *bn = plan.bn;
     *cta_pair = plan.pair ? 1 : 0;
     if (resident_units)
         *resident_units = plan.resident;
+    if (k_split)
+        *k_split = plan.split;
     return CK_OK;
 }
 

@@ -17,6 +17,7 @@ enum : uint32_t {
     kErrWaitDrain = 1u << 3,     // teardown gave up waiting for in-flight copies / MMAs
     kErrWaitSelfTest = 1u << 4,  // the wait self-test timed out (expected by that test)
     kErrWaitGrid = 1u << 5,      // a grid-wide barrier of a preparation kernel timed out
+    kErrTailCount = 1u << 6,     // a K-split tail unit's arrival counter kept changing (not expected)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
@@ -107,6 +108,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// ---------------------------------------------------------------- register re-balancing
+// Executed by every thread of a warpgroup (4 consecutive warps): release registers to,
+// or claim them from, the block's pool.  An increase waits until the pool can serve it,
+// so the caller must make sure the launch provides the sum of the final counts.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
 {
@@ -156,6 +175,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
                  "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+
+// 1-D bulk copy from global memory into this CTA's shared memory; the bytes complete on
+// `bar` (both addresses 16-byte aligned, `bytes` a multiple of 16).
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
 

@@ -45,6 +45,7 @@ struct GemmProblem {
     int scalar_scales = 0;
     void* y = nullptr;           // [M,N] of the output type
     int out_dtype = 0;           // 0 bf16, 1 fp16, 2 fp32
+    void* tail = nullptr;        // gemm_tail_bytes(M, N) bytes of workspace (K-split tail)
     int32_t* acc = nullptr;      // int32 [M,N]
 };
 
@@ -59,14 +60,35 @@ cudaError_t current_device(DeviceInfo* info);
 
 // Kernel launchers.  Each returns cudaSuccess or the launch error; `why` gets a
 // description of a failure that is not a CUDA error.
-// The GEMM launch configuration for an M x N output: CTA pairs or single CTAs, the tile
-// width (a multiple of 32 up to 256) and how many units can be resident at once.
+// The GEMM's K-split tail keeps, per CTA slice of a split unit, 128 x 256 int32 partial
+// sums and 8 arrival slots of 16 bytes in the caller's workspace; at most
+// gemm_tail_ctas(M, N) CTA slices, a bound that needs no device query.
+constexpr int kTailMaxSplit = 8;
+constexpr int64_t kTailMaxCtas = 152;
+constexpr size_t kTailCtaBytes = (size_t)128 * 256 * 4;
+constexpr size_t kTailSlotBytesPerCta = (size_t)8 * 16;
+inline int64_t gemm_tail_ctas(int64_t M, int64_t N)
+{
+    const int64_t slices = ((M + 127) / 128) * ((N + 31) / 32) * kTailMaxSplit;
+    return slices < kTailMaxCtas ? slices : kTailMaxCtas;
+}
+inline size_t gemm_tail_bytes(int64_t M, int64_t N)
+{
+    return (size_t)gemm_tail_ctas(M, N) * (kTailCtaBytes + kTailSlotBytesPerCta);
+}
+
+// The GEMM launch configuration for an M x N x K problem: CTA pairs or single CTAs, the
+// tile width (a multiple of 32 up to 256), how many units can be resident at once, and
+// the K-split of the last partial wave (split = 1: none).
 struct GemmPlan {
     bool pair = false;
     int bn = 0;
     int64_t resident = 0;
+    int64_t units = 0;       // units of the whole problem
+    int64_t full_units = 0;  // units computed whole; the rest are split
+    int split = 1;
 };
-cudaError_t plan_gemm(int64_t M, int64_t N, const DeviceInfo& dev, GemmPlan* plan);
+cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev, GemmPlan* plan);
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why);
 cudaError_t launch_quantize_rows(const void* x, int64_t M, int64_t K, bool rotate, int8_t* q8, void* q16,
                                  float* x_scale, const DeviceInfo& dev, cudaStream_t s);

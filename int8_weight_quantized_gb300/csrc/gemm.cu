@@ -38,10 +38,14 @@
 // from L2.  Every wait is bounded (see mbar_wait); a timed-out CTA records an error bit,
 // lets its copies and MMAs finish, frees TMEM and exits.
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+
+#include <unistd.h>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -64,7 +68,14 @@ constexpr int BK = 64;        // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;    // K per kind::f16 instruction
 constexpr int CHUNK_KB = 16;  // k-blocks per exact fp32 chunk (16 * 64 = 1024 products)
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 32 * (2 + EPI_WARPS);
+constexpr int EPI_WARP0 = 4;                  // warps 0-3: producer, MMA issuer, two idle
+constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+// Registers per thread after the warpgroups re-balance (setmaxnreg): the first
+// warpgroup needs few, the two epilogue warpgroups hold 128 running sums per thread.
+// The launch must provide at least their sum (checked on the host before launching).
+constexpr uint32_t REGS_WG0 = 56;
+constexpr uint32_t REGS_EPI = 216;
+constexpr uint32_t REGS_NEEDED_PER_BLOCK = 128 * REGS_WG0 + 256 * REGS_EPI;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr int B_BOX_ROWS = BN / 2;                       // most weight rows per TMA box
 constexpr uint32_t B_BOX_BYTES = B_BOX_ROWS * BK * 2;
@@ -101,7 +112,67 @@ struct Args {
     int units_m, tiles_m, tiles_n, num_kb, group_m;
     int scalar_scales;
     uint64_t timeout_ns;
+    // K-split of the last partial wave: units [full_units, num_units) are each computed
+    // as `split` K-slices by different units of the grid; every slice writes its int32
+    // running sums to `partials`, and the slice that arrives last at the unit's counter
+    // in `tail_slots` adds the others' sums and runs the epilogue.
+    int64_t full_units;
+    int64_t num_items;      // full_units + (num_units - full_units) * split
+    int split;              // 1 = no split
+    int32_t* partials;      // [tail unit][slice][rank][epilogue warp][column group of 4][lane][4] int32
+    unsigned long long* tail_slots;  // [tail unit][rank][epilogue warp] (tag << 16) | arrivals, 16 bytes apart
+    unsigned long long epoch;        // this launch's tag for tail_slots
 };
+
+// One work item of the persistent loop: a whole unit, or one K-slice of a tail unit.
+struct Item {
+    int64_t unit;
+    int64_t tail;   // index among the tail units (slice >= 0 only)
+    int kb_begin, kb_end;
+    int slice;      // -1: the whole K range
+};
+
+__device__ __forceinline__ Item item_of(int64_t it, const Args& a)
+{
+    Item r;
+    if (it < a.full_units) {
+        r.unit = it;
+        r.tail = 0;
+        r.kb_begin = 0;
+        r.kb_end = a.num_kb;
+        r.slice = -1;
+    } else {
+        const int64_t j = it - a.full_units;
+        r.tail = j / a.split;
+        r.slice = (int)(j - r.tail * a.split);
+        r.unit = a.full_units + r.tail;
+        r.kb_begin = (int)((int64_t)a.num_kb * r.slice / a.split);
+        r.kb_end = (int)((int64_t)a.num_kb * (r.slice + 1) / a.split);
+    }
+    return r;
+}
+
+// Count one arrival at a tail unit's 64-bit slot, packed as (launch tag << 16) | count:
+// a slot still tagged by an earlier launch (or holding anything else) restarts at 1.
+// The tag is the launch's 64-bit epoch cut to 48 bits, so stale or random slot contents
+// match it with probability 2^-48.  Returns true for the arrival that makes the count
+// `split`.  Each failed swap means another arrival went in (or the first read was
+// stale), so the retries are bounded.
+__device__ __forceinline__ bool tail_arrive(unsigned long long* slot, unsigned long long epoch, int split,
+                                            unsigned int* err)
+{
+    const unsigned long long tag = epoch & 0xFFFFFFFFFFFFull;
+    unsigned long long old = __ldcg(slot);
+    for (int i = 0; i < 4 * split + 8; ++i) {
+        const unsigned long long count = (old >> 16) == tag ? (old & 0xFFFFull) + 1 : 1;
+        const unsigned long long prev = atomicCAS(slot, old, (tag << 16) | count);
+        if (prev == old)
+            return count == (unsigned long long)split;
+        old = prev;
+    }
+    atomicOr(err, kErrTailCount);
+    return false;
+}
 
 // Unit u (a pair-tile, or a tile) -> (unit row, tile column) in grouped order.
 __device__ __forceinline__ void unit_coords(int64_t u, const Args& a, int& um, int& nb)
@@ -155,8 +226,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     }
 }
 
-// 10 warps put three warps on two of the four SM sub-partitions, whose register files
-// hold 16K registers each: at most 168 registers per thread.
+// 12 warps put three warps on each of the four SM sub-partitions, whose register files
+// hold 16K registers each: at most 168 registers per thread at launch, re-balanced to
+// REGS_WG0 / REGS_EPI once the roles split (32 x (56 + 2 x 216) <= 16K per
+// sub-partition as well).
 template <bool RAW, bool PAIR, int OUT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -223,122 +296,128 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     // everything above overlapped the previous kernel; from here on global memory is read
     griddep_wait();
-
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_mask = 0;       // stages holding a load
-            uint32_t issued_parity = 0;     // parity of that load's phase, per stage
-            bool ok = true;
-            for (int64_t u = cluster; ok && u < args.num_units; u += clusters) {
-                int um, nb;
-                unit_coords(u, args, um, nb);
-                const int32_t m0 = (um * args.unit_rows + rank) * BM, n0 = nb * args.bn;
-                const int half_rows = args.bn >> 1;  // weight rows per box
-                for (int kb = 0; kb < args.num_kb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kErrWaitProducer, args.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* sa = s_ab + (size_t)stage * MD::STAGE_BYTES;
-                    uint8_t* sb = sa + A_BYTES;
-                    if (PAIR) {
-                        // both CTAs' bytes are counted on the leader's barrier
-                        const uint32_t bar = mapa_shared(&full[stage], 0);
-                        if (leader)
-                            mbar_arrive_expect_tx(&full[stage], args.tx_bytes);
-                        tma_load_2d_pair(sa, &tmA, bar, kb * BK, m0);
-                        tma_load_2d_pair(sb, &tmB, bar, kb * BK, n0 + rank * half_rows);
-                    } else {
-                        mbar_arrive_expect_tx(&full[stage], args.tx_bytes);
-                        tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
-                        tma_load_2d(sb, &tmB, &full[stage], kb * BK, n0);
-                        tma_load_2d(sb + half_rows * BK * 2, &tmB, &full[stage], kb * BK, n0 + half_rows);
-                    }
-                    issued_mask |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok && leader) {
-                // the CTA is aborting: let every issued copy land before shared memory is
-                // released (the leader's barriers count both CTAs' bytes)
-                for (int s = 0; s < STAGES; ++s)
-                    if (issued_mask & (1u << s))
-                        drain_wait(&full[s], (issued_parity >> s) & 1u, err, args.timeout_ns);
-            }
-        }
-        __syncwarp();  // reconverge before the block-wide barrier below
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && leader) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t acc_iter = 0;
-            bool ok = true;
-            for (int64_t u = cluster; ok && u < args.num_units; u += clusters) {
-                for (int kb0 = 0; kb0 < args.num_kb; kb0 += CHUNK_KB) {
-                    const uint32_t buf = acc_iter & 1u;
-                    const uint32_t acc_phase = (acc_iter >> 1) & 1u;
-                    if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort_flag, err, kErrWaitMma, args.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + buf * BN;
-                    const int kend = min(kb0 + CHUNK_KB, args.num_kb);
-                    for (int kb = kb0; kb < kend; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, abort_flag, err, kErrWaitMma, args.timeout_ns)) {
+    if (warp < EPI_WARP0) {
+        // ---------------------------------------------------------------- warpgroup 0
+        setmaxnreg_dec<REGS_WG0>();
+        if (warp == 0) {
+            // ------------------------------------------------------------ TMA producer
+            if (lane == 0) {
+                int stage = 0;
+                uint32_t phase = 0;
+                uint32_t issued_mask = 0;       // stages holding a load
+                uint32_t issued_parity = 0;     // parity of that load's phase, per stage
+                bool ok = true;
+                for (int64_t it = cluster; ok && it < args.num_items; it += clusters) {
+                    const Item w = item_of(it, args);
+                    int um, nb;
+                    unit_coords(w.unit, args, um, nb);
+                    const int32_t m0 = (um * args.unit_rows + rank) * BM, n0 = nb * args.bn;
+                    const int half_rows = args.bn >> 1;  // weight rows per box
+                    for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kErrWaitProducer, args.timeout_ns)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        const uint32_t a0 = smem_u32(s_ab + (size_t)stage * MD::STAGE_BYTES);
-                        const uint32_t b0 = a0 + A_BYTES;
-#pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k) {
-                            // +32 bytes per 16-element K step inside the 128-byte swizzle row
-                            const uint64_t ad = desc_kmajor_sw128(a0 + k * 32), bd = desc_kmajor_sw128(b0 + k * 32);
-                            const uint32_t accumulate = (kb > kb0 || k > 0) ? 1u : 0u;
-                            if (PAIR)
-                                mma_bf16_pair(d_tmem, ad, bd, args.idesc, accumulate);
-                            else
-                                mma_bf16(d_tmem, ad, bd, args.idesc, accumulate);
+                        uint8_t* sa = s_ab + (size_t)stage * MD::STAGE_BYTES;
+                        uint8_t* sb = sa + A_BYTES;
+                        if (PAIR) {
+                            // both CTAs' bytes are counted on the leader's barrier
+                            const uint32_t bar = mapa_shared(&full[stage], 0);
+                            if (leader)
+                                mbar_arrive_expect_tx(&full[stage], args.tx_bytes);
+                            tma_load_2d_pair(sa, &tmA, bar, kb * BK, m0);
+                            tma_load_2d_pair(sb, &tmB, bar, kb * BK, n0 + rank * half_rows);
+                        } else {
+                            mbar_arrive_expect_tx(&full[stage], args.tx_bytes);
+                            tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
+                            tma_load_2d(sb, &tmB, &full[stage], kb * BK, n0);
+                            tma_load_2d(sb + half_rows * BK * 2, &tmB, &full[stage], kb * BK, n0 + half_rows);
                         }
-                        if (PAIR)
-                            mma_commit_pair(&empty[stage], kPairMask);  // frees the stage in both CTAs
-                        else
-                            mma_commit(&empty[stage]);
+                        issued_mask |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
-                    if (!ok)
-                        break;
-                    if (PAIR)
-                        mma_commit_pair(&acc_full[buf], kPairMask);
-                    else
-                        mma_commit(&acc_full[buf]);
-                    ++acc_iter;
+                }
+                if (!ok && leader) {
+                    // the CTA is aborting: let every issued copy land before shared memory is
+                    // released (the leader's barriers count both CTAs' bytes)
+                    for (int s = 0; s < STAGES; ++s)
+                        if (issued_mask & (1u << s))
+                            drain_wait(&full[s], (issued_parity >> s) & 1u, err, args.timeout_ns);
                 }
             }
-            // every MMA issued above must be complete before TMEM is released
-            if (PAIR)
-                mma_commit_pair(drain, 0x1);
-            else
-                mma_commit(drain);
-            drain_wait(drain, 0, err, args.timeout_ns);
+            __syncwarp();  // reconverge before the block-wide barrier below
+        } else if (warp == 1) {
+            // ------------------------------------------------------------ MMA issuer
+            if (lane == 0 && leader) {
+                int stage = 0;
+                uint32_t phase = 0;
+                uint32_t acc_iter = 0;
+                bool ok = true;
+                for (int64_t it = cluster; ok && it < args.num_items; it += clusters) {
+                    const Item w = item_of(it, args);
+                    for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += CHUNK_KB) {
+                        const uint32_t buf = acc_iter & 1u;
+                        const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                        if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort_flag, err, kErrWaitMma, args.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem_base + buf * BN;
+                        const int kend = min(kb0 + CHUNK_KB, w.kb_end);
+                        for (int kb = kb0; kb < kend; ++kb) {
+                            if (!mbar_wait(&full[stage], phase, abort_flag, err, kErrWaitMma, args.timeout_ns)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t a0 = smem_u32(s_ab + (size_t)stage * MD::STAGE_BYTES);
+                            const uint32_t b0 = a0 + A_BYTES;
+    #pragma unroll
+                            for (int k = 0; k < BK / UMMA_K; ++k) {
+                                // +32 bytes per 16-element K step inside the 128-byte swizzle row
+                                const uint64_t ad = desc_kmajor_sw128(a0 + k * 32), bd = desc_kmajor_sw128(b0 + k * 32);
+                                const uint32_t accumulate = (kb > kb0 || k > 0) ? 1u : 0u;
+                                if (PAIR)
+                                    mma_bf16_pair(d_tmem, ad, bd, args.idesc, accumulate);
+                                else
+                                    mma_bf16(d_tmem, ad, bd, args.idesc, accumulate);
+                            }
+                            if (PAIR)
+                                mma_commit_pair(&empty[stage], kPairMask);  // frees the stage in both CTAs
+                            else
+                                mma_commit(&empty[stage]);
+                            if (++stage == STAGES) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                        if (!ok)
+                            break;
+                        if (PAIR)
+                            mma_commit_pair(&acc_full[buf], kPairMask);
+                        else
+                            mma_commit(&acc_full[buf]);
+                        ++acc_iter;
+                    }
+                }
+                // every MMA issued above must be complete before TMEM is released
+                if (PAIR)
+                    mma_commit_pair(drain, 0x1);
+                else
+                    mma_commit(drain);
+                drain_wait(drain, 0, err, args.timeout_ns);
+            }
+            __syncwarp();  // reconverge before the block-wide barrier below
         }
-        __syncwarp();  // reconverge before the block-wide barrier below
     } else {
-        // ------------------------------------------------------------ epilogue
-        const int e = warp - 2;
+        // ---------------------------------------------------------------- epilogue
+        setmaxnreg_inc<REGS_EPI>();
+        const int e = warp - EPI_WARP0;
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int half = e >> 2;       // which 128 of the 256 tile columns
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -346,18 +425,30 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t acc_iter = 0;
         uint32_t nstore = 0;
         bool ok = true;
-        for (int64_t u = cluster; ok && u < args.num_units; u += clusters) {
+        for (int64_t it = cluster; ok && it < args.num_items; it += clusters) {
+            const Item w = item_of(it, args);
             int um, nb;
-            unit_coords(u, args, um, nb);
+            unit_coords(w.unit, args, um, nb);
             const int64_t m0 = (int64_t)(um * args.unit_rows + rank) * BM;
             const int64_t n0 = (int64_t)nb * args.bn;
             // columns of the tile in this warp's half: a multiple of 32 in [0, 128]
             const int ncols = max(0, min(128, args.bn - half * 128));
+            const int64_t row = m0 + quarter * 32 + lane;
+            const int64_t cbase = n0 + half * 128;
+            float xsv = 0.0f, ws_scalar = 0.0f;
+            if (!RAW) {  // the scalar scales and this lane's row scale, in flight during the K loop
+                if (args.scalar_scales) {
+                    ws_scalar = __ldg(args.ws);
+                    xsv = __ldg(args.xs);
+                } else if (row < args.M) {
+                    xsv = __ldg(args.xs + row);
+                }
+            }
             int32_t run[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j)
                 run[j] = 0;
-            for (int kb0 = 0; kb0 < args.num_kb; kb0 += CHUNK_KB) {
+            for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += CHUNK_KB) {
                 const uint32_t buf = acc_iter & 1u;
                 const uint32_t acc_phase = (acc_iter >> 1) & 1u;
                 // one lane polls, the warp follows its verdict (keeps the warp converged
@@ -396,8 +487,47 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok)
                 break;
 
-            const int64_t row = m0 + quarter * 32 + lane;
-            const int64_t cbase = n0 + half * 128;
+            if (w.slice >= 0 && ncols > 0) {
+                // one K-slice of a tail unit: publish this warp's sums; the last slice to
+                // arrive adds the others' and goes on to the epilogue
+                constexpr int RANKS = PAIR ? 2 : 1;
+                const int lslot = rank * EPI_WARPS + e;                       // this warp within the unit
+                const int64_t wslot = w.tail * (RANKS * EPI_WARPS) + lslot;   // its arrival counter
+                const int64_t span = (int64_t)RANKS * EPI_WARPS * 32 * 128;   // int32 per slice
+                // a warp's sums are 32 column groups of 4, each stored as 32 lanes x 16 bytes
+                // in a row, so every store and load of a warp covers 512 contiguous bytes
+                int32_t* mine = args.partials + (w.tail * args.split + w.slice) * span + lslot * (32 * 128) + lane * 4;
+#pragma unroll
+                for (int c4 = 0; c4 < 32; ++c4)
+                    if (4 * c4 < ncols)
+                        __stcg(reinterpret_cast<int4*>(mine + c4 * 128),
+                               make_int4(run[4 * c4], run[4 * c4 + 1], run[4 * c4 + 2], run[4 * c4 + 3]));
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0)
+                    last = tail_arrive(args.tail_slots + 2 * wslot, args.epoch, args.split, err) ? 1 : 0;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (!last)
+                    continue;  // another slice stores the unit
+                __threadfence();  // the other slices' sums, published before their arrivals
+                for (int sl = 0; sl < args.split; ++sl) {
+                    if (sl == w.slice)
+                        continue;
+                    const int32_t* other =
+                        args.partials + (w.tail * args.split + sl) * span + lslot * (32 * 128) + lane * 4;
+#pragma unroll
+                    for (int c4 = 0; c4 < 32; ++c4)
+                        if (4 * c4 < ncols) {
+                            const int4 v = __ldcg(reinterpret_cast<const int4*>(other + c4 * 128));
+                            run[4 * c4] += v.x;
+                            run[4 * c4 + 1] += v.y;
+                            run[4 * c4 + 2] += v.z;
+                            run[4 * c4 + 3] += v.w;
+                        }
+                }
+            }
+
             if (RAW) {
                 if (row < args.M) {
                     int32_t* dst = args.acc + row * args.N;
@@ -413,8 +543,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
                 using OT = OutType<OUT>;
                 constexpr int PC = OT::PER_CHUNK;
-                const bool row_ok = row < args.M;
-                const float xsv = args.scalar_scales ? args.xs[0] : (row_ok ? args.xs[row] : 0.0f);
                 const int64_t row0 = m0 + quarter * 32;
 #pragma unroll
                 for (int g = 0; g < 128 / OT::BOX_COLS; ++g) {
@@ -427,38 +555,32 @@ __global__ void __launch_bounds__(THREADS, 1)
                     __syncwarp();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {  // one 16-byte chunk of the row: PC columns
-                        const int64_t col = col0 + c * PC;
                         const int j0 = g * OT::BOX_COLS + c * PC;  // first running sum of the chunk
+                        const int64_t col = col0 + c * PC;
+                        // the same columns for every lane: broadcast loads, L1 hits after the
+                        // first tile of a column range
                         float wsv[PC], bv[PC];
                         if (col < args.N) {  // N % 8 == 0: a chunk is all in or all out
-                            if (args.scalar_scales) {
 #pragma unroll
-                                for (int i = 0; i < PC; ++i)
-                                    wsv[i] = args.ws[0];
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < PC; i += 4) {
-                                    const float4 w4 = *reinterpret_cast<const float4*>(args.ws + col + i);
-                                    wsv[i] = w4.x; wsv[i + 1] = w4.y; wsv[i + 2] = w4.z; wsv[i + 3] = w4.w;
-                                }
-                            }
-                            if (args.bias) {
-                                if (PC == 8) {
-                                    const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + col);
-                                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&braw);
-#pragma unroll
-                                    for (int i = 0; i < PC / 2; ++i) {
-                                        bv[2 * i] = __low2float(b2[i]);
-                                        bv[2 * i + 1] = __high2float(b2[i]);
-                                    }
+                            for (int h = 0; h < PC / 4; ++h) {
+                                if (args.scalar_scales) {
+                                    wsv[4 * h] = wsv[4 * h + 1] = wsv[4 * h + 2] = wsv[4 * h + 3] = ws_scalar;
                                 } else {
-                                    const uint2 braw = *reinterpret_cast<const uint2*>(args.bias + col);
+                                    const float4 w4 = __ldg(reinterpret_cast<const float4*>(args.ws + col + 4 * h));
+                                    wsv[4 * h] = w4.x;
+                                    wsv[4 * h + 1] = w4.y;
+                                    wsv[4 * h + 2] = w4.z;
+                                    wsv[4 * h + 3] = w4.w;
+                                }
+                                if (args.bias) {
+                                    const uint2 braw = __ldg(reinterpret_cast<const uint2*>(args.bias + col + 4 * h));
                                     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&braw);
-#pragma unroll
-                                    for (int i = 0; i < PC / 2; ++i) {
-                                        bv[2 * i] = __low2float(b2[i]);
-                                        bv[2 * i + 1] = __high2float(b2[i]);
-                                    }
+                                    bv[4 * h] = __low2float(b2[0]);
+                                    bv[4 * h + 1] = __high2float(b2[0]);
+                                    bv[4 * h + 2] = __low2float(b2[1]);
+                                    bv[4 * h + 3] = __high2float(b2[1]);
+                                } else {
+                                    bv[4 * h] = bv[4 * h + 1] = bv[4 * h + 2] = bv[4 * h + 3] = 0.0f;
                                 }
                             }
                         } else {  // past the last column: computed, then clipped by the store
@@ -500,8 +622,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         }
+        // the stores must have read shared memory before it is released; their writes to
+        // global memory complete with the grid
         if (lane == 0)
-            bulk_wait_group<0>();
+            bulk_wait_group_read<0>();
         __syncwarp();
     }
 
@@ -593,6 +717,16 @@ static cudaError_t ensure_smem_attr(int device)
     cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR, OUT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)gemm::Mode<PAIR>::SMEM_BYTES);
+    if (e == cudaSuccess) {
+        // the warpgroups' register re-balancing must fit in what a block is launched
+        // with (registers are granted per warp in units of 8 per thread), else the
+        // epilogue's increase would wait forever: refuse to launch instead
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<RAW, PAIR, OUT>);
+        if (e == cudaSuccess &&
+            (uint64_t)((fa.numRegs + 7) / 8 * 8) * gemm::THREADS < (uint64_t)gemm::REGS_NEEDED_PER_BLOCK)
+            e = cudaErrorInvalidConfiguration;
+    }
     if (e == cudaSuccess && device >= 0 && device < 64)
         done[device] = true;
     return e;
@@ -655,19 +789,66 @@ static int64_t kblock_cost(bool pair, int bn)
     return pair ? 30500 + 15 * (int64_t)bn : 30000 + 29 * (int64_t)bn;
 }
 
-// The configuration that finishes soonest: `units` = rows of units times ceil(N / bn)
-// columns run in ceil(units / resident) waves of kblock_cost() each.
-// CK_GEMM_BN=<width> forces a width (A/B timing).
-static void choose_tile(int64_t N, int64_t tiles_m, int64_t resident_pair, int64_t resident_single,
-                        bool pair_allowed, bool single_allowed, GemmPlan* plan)
+// A K-split tail slice must keep at least this many k-blocks.  Publishing the slices'
+// sums (write, fence, count the arrival) and adding them in the last slice cost, as
+// measured on GB300 (2-, 3- and 4-way splits of 64- and 48-k-block units), about
+// kSplitFixedKb + kSplitPerSliceKb * split k-block times.
+constexpr int kMinSliceKb = 4;
+constexpr int64_t kSplitFixedKb = 10;
+constexpr int64_t kSplitPerSliceKb = 10;
+
+// Cost of one configuration: `units` run as waves of `resident`; the last partial wave,
+// if any, either runs whole or is split `split` ways along K over the idle units.
+struct TileCost {
+    int64_t cost;
+    int split;
+    int64_t full_units;
+};
+
+static TileCost tile_cost(bool pair, int bn, int64_t units, int64_t resident, int num_kb, int64_t tail_ctas,
+                          int force_split)
 {
-    int force_bn = 0;
-    if (const char* force = std::getenv("CK_GEMM_BN")) {
-        const int f = std::atoi(force);
-        if (f >= 32 && f <= gemm::BN && f % 32 == 0)
-            force_bn = f;
+    const int64_t waves = units / resident, tail = units % resident;
+    TileCost c{(waves + (tail ? 1 : 0)) * num_kb, 1, units};
+    if (tail && force_split != 1) {
+        const int64_t ranks = pair ? 2 : 1;
+        const int64_t smax = std::min(std::min(resident / tail, (int64_t)(num_kb / kMinSliceKb)),
+                                      std::min((int64_t)kTailMaxSplit, tail_ctas / (tail * ranks)));
+        for (int sp = 2; sp <= smax; ++sp) {
+            if (force_split > 1 && sp != force_split)
+                continue;
+            const int64_t kbs = waves * num_kb + (num_kb + sp - 1) / sp + kSplitFixedKb + kSplitPerSliceKb * sp;
+            if (kbs < c.cost || force_split > 1) {
+                c.cost = kbs;
+                c.split = sp;
+                c.full_units = waves * resident;
+            }
+        }
     }
+    c.cost *= kblock_cost(pair, bn);
+    return c;
+}
+
+// The configuration that finishes soonest.  CK_GEMM_BN=<width> forces a width,
+// CK_GEMM_SPLIT=1 turns the K-split tail off and CK_GEMM_SPLIT=<s> asks for s slices
+// where the tail allows it (A/B timing).
+static void choose_tile(int64_t M, int64_t N, int num_kb, int64_t tiles_m, int64_t resident_pair,
+                        int64_t resident_single, bool pair_allowed, bool single_allowed, GemmPlan* plan)
+{
+    int force_bn = 0, force_split = 0;
+    if (const char* f = std::getenv("CK_GEMM_BN")) {
+        const int v = std::atoi(f);
+        if (v >= 32 && v <= gemm::BN && v % 32 == 0)
+            force_bn = v;
+    }
+    if (const char* f = std::getenv("CK_GEMM_SPLIT")) {
+        const int v = std::atoi(f);
+        if (v >= 1 && v <= kTailMaxSplit)
+            force_split = v;
+    }
+    const int64_t tail_ctas = gemm_tail_ctas(M, N);
     int64_t best_cost = -1;
+    bool best_forced = false;  // the best so far has the requested split
     for (int p = pair_allowed ? 1 : 0; p >= (single_allowed ? 0 : 1); --p) {
         const int64_t units_m = p ? (tiles_m + 1) / 2 : tiles_m;
         const int64_t resident = p ? resident_pair : resident_single;
@@ -675,13 +856,20 @@ static void choose_tile(int64_t N, int64_t tiles_m, int64_t resident_pair, int64
             if (force_bn && bn != force_bn)
                 continue;
             const int64_t units = units_m * ((N + bn - 1) / bn);
-            const int64_t waves = (units + resident - 1) / resident;
-            const int64_t cost = waves * kblock_cost(p != 0, bn);
-            if (best_cost < 0 || cost < best_cost) {
-                best_cost = cost;
+            const TileCost c = tile_cost(p != 0, bn, units, resident, num_kb, tail_ctas, force_split);
+            // a requested split wins over cheaper configurations that cannot have it
+            const bool forced = force_split > 1 && c.split == force_split;
+            if (best_forced && !forced)
+                continue;
+            if (best_cost < 0 || c.cost < best_cost || (forced && !best_forced)) {
+                best_forced = forced;
+                best_cost = c.cost;
                 plan->pair = p != 0;
                 plan->bn = bn;
                 plan->resident = resident;
+                plan->units = units;
+                plan->full_units = c.full_units;
+                plan->split = c.split;
             }
         }
     }
@@ -702,12 +890,30 @@ static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB,
         return e;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config(PAIR, Mode<PAIR>::SMEM_BYTES, s, attr);
-    const int64_t units = std::min<int64_t>(a.num_units, resident);
+    const int64_t units = std::min<int64_t>(a.num_items, resident);
     cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units));
     return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR, OUT>, tmA, tmB, tmY, a);
 }
 
-cudaError_t plan_gemm(int64_t M, int64_t N, const DeviceInfo& dev, GemmPlan* plan)
+// A 64-bit tag no earlier launch of this process used (high-entropy start, so slots
+// left in recycled memory by another process do not match either); never 0.
+static unsigned long long next_gemm_epoch()
+{
+    static std::atomic<unsigned long long> counter([] {
+        unsigned long long z = (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() ^
+                               ((unsigned long long)getpid() << 31) ^ 0xD1B54A32D192ED03ull;
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;  // splitmix64 finaliser
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        return z ^ (z >> 31);
+    }());
+    unsigned long long e;
+    do {
+        e = counter.fetch_add(1, std::memory_order_relaxed);
+    } while (e == 0);
+    return e;
+}
+
+cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev, GemmPlan* plan)
 {
     const int64_t tiles_m = (M + gemm::BM - 1) / gemm::BM;
     // CK_GEMM_PAIR=0 / =1 restricts the choice to single CTAs / CTA pairs (A/B timing);
@@ -721,7 +927,8 @@ cudaError_t plan_gemm(int64_t M, int64_t N, const DeviceInfo& dev, GemmPlan* pla
         e = resident_units<true>(dev, &resident_pair);
     if (e != cudaSuccess)
         return e;
-    choose_tile(N, tiles_m, resident_pair, resident_single, pair_allowed, single_allowed, plan);
+    const int num_kb = (int)((K + gemm::BK - 1) / gemm::BK);
+    choose_tile(M, N, num_kb, tiles_m, resident_pair, resident_single, pair_allowed, single_allowed, plan);
     return cudaSuccess;
 }
 
@@ -762,7 +969,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.scalar_scales = p.scalar_scales;
     a.timeout_ns = DEFAULT_TIMEOUT_NS;
     GemmPlan plan;
-    const cudaError_t e = plan_gemm(p.M, p.N, dev, &plan);
+    const cudaError_t e = plan_gemm(p.M, p.N, p.K, dev, &plan);
     if (e != cudaSuccess)
         return e;
     const bool pair = plan.pair;
@@ -772,6 +979,21 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.bn = plan.bn;
     a.tiles_n = (int)((p.N + a.bn - 1) / a.bn);
     a.num_units = (int64_t)a.units_m * a.tiles_n;
+    a.split = 1;
+    a.full_units = a.num_units;
+    a.num_items = a.num_units;
+    a.partials = nullptr;
+    a.tail_slots = nullptr;
+    a.epoch = 0;
+    if (plan.split > 1 && p.tail != nullptr && plan.units == a.num_units) {
+        const int64_t ctas = gemm_tail_ctas(p.M, p.N);
+        a.split = plan.split;
+        a.full_units = plan.full_units;
+        a.num_items = a.full_units + (a.num_units - a.full_units) * a.split;
+        a.partials = static_cast<int32_t*>(p.tail);
+        a.tail_slots = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(p.tail) + ctas * kTailCtaBytes);
+        a.epoch = next_gemm_epoch();
+    }
     a.idesc = (pair ? Mode<true>::IDESC_M : Mode<false>::IDESC_M) | ((uint32_t)(a.bn >> 3) << 17);
     a.tx_bytes = (pair ? 2u : 1u) * (A_BYTES + (uint32_t)(pair ? a.bn / 2 : a.bn) * BK * 2);
     if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.b, p.K, p.N, (uint64_t)p.K * 2, BK, a.bn / 2,

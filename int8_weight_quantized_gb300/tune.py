@@ -2,7 +2,8 @@
 
 For each M x N x K problem the GEMM is timed with every tile configuration it supports
 (CTA pairs with 256-row tiles or single CTAs with 128-row tiles, times tile widths 32,
-64, ..., 256 output columns) and with the configuration the library picks by itself
+64, ..., 256 output columns; each without and, where the last wave is partial, with the
+K-split of that wave) and with the configuration the library picks by itself
 (ck_gemm_tile_config).  The report gives, per shape, the picked and the best
 configuration and the regret of the pick: the per-shape tile sweep of the comfy-kitchen
 pages (issue #280, "Kernel used": one fixed config found best on every H3 shape; the
@@ -13,8 +14,9 @@ the library's own per-launch choice.
                                              [--json out.json] [--markdown out.md]
 
 Only the GEMM kernel is timed (CUDA events around it, via ck_profile_begin); L2 is
-flushed before every timed launch.  Forcing a configuration uses the library's A/B
-overrides CK_GEMM_PAIR / CK_GEMM_BN, set in this process's environment.
+flushed before every timed launch (a 512 MiB write, then a 256 MiB read so no dirty
+lines are left to write back).  Forcing a configuration uses the library's A/B
+overrides CK_GEMM_PAIR / CK_GEMM_BN / CK_GEMM_SPLIT, set in this process's environment.
 """
 import argparse
 import json
@@ -32,6 +34,7 @@ DEFAULT_SHAPES = [
 ]
 WIDTHS = list(range(256, 0, -32))
 FLUSH_BYTES = 512 << 20
+CLEAN_BYTES = 256 << 20
 
 
 def parse_shapes(text):
@@ -42,23 +45,29 @@ def parse_shapes(text):
     return out
 
 
-def _set_override(pair, bn):
-    for key, val in (("CK_GEMM_PAIR", pair), ("CK_GEMM_BN", bn)):
+def _set_override(pair, bn, split=None):
+    for key, val in (("CK_GEMM_PAIR", pair), ("CK_GEMM_BN", bn), ("CK_GEMM_SPLIT", split)):
         if val is None:
             os.environ.pop(key, None)
         else:
             os.environ[key] = str(val)
 
 
-def time_config(args, flush, pair, bn, reps, warmup=2):
-    """Median GEMM milliseconds with the configuration forced (None = the library's pick)."""
-    _set_override(None if pair is None else (1 if pair else 0), bn)
+def flush_l2(flush):
+    flush[0].zero_()
+    torch.sum(flush[1], dim=0, out=flush[2])
+
+
+def time_config(args, flush, pair, bn, reps, split=None, warmup=2):
+    """Median GEMM milliseconds with the configuration forced (None = the library's pick;
+    split=1 turns the K-split of the last partial wave off)."""
+    _set_override(None if pair is None else (1 if pair else 0), bn, split)
     try:
         for _ in range(warmup):
             ck_int8_gemm_dequant(*args)
         times = []
         for _ in range(reps):
-            flush.zero_()
+            flush_l2(flush)
             ck_profile_begin(with_events=True)
             ck_int8_gemm_dequant(*args)
             times.append(ck_profile_end()["gemm"][0])
@@ -75,12 +84,18 @@ def sweep_shape(M, N, K, reps, flush, seed=7):
     ws = synthetic.scale_uniform(N, seed + 3, mul=0.01, device=dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     args = (q, xs, w, ws, None, False, y)
-    pick_bn, pick_pair, resident = ck_gemm_tile_config(M, N, K)
+    pick_bn, pick_pair, resident, pick_split = ck_gemm_tile_config(M, N, K)
     configs = {}
     pairs = [True, False] if (M + 127) // 128 >= 2 else [False]
     for pair in pairs:
         for bn in WIDTHS:
-            configs["%s/%d" % ("pair" if pair else "single", bn)] = time_config(args, flush, pair, bn, reps)
+            name = "%s/%d" % ("pair" if pair else "single", bn)
+            configs[name] = time_config(args, flush, pair, bn, reps, split=1)
+            _set_override(1 if pair else 0, bn)
+            split = ck_gemm_tile_config(M, N, K)[3]
+            _set_override(None, None)
+            if split > 1:
+                configs["%s/split%d" % (name, split)] = time_config(args, flush, pair, bn, reps)
     picked_ms = time_config(args, flush, None, None, reps)
     best = min(configs, key=configs.get)
     flops = 2.0 * M * N * K
@@ -88,7 +103,8 @@ def sweep_shape(M, N, K, reps, flush, seed=7):
     torch.cuda.empty_cache()
     return {
         "shape": [M, N, K],
-        "picked": "%s/%d" % ("pair" if pick_pair else "single", pick_bn),
+        "picked": "%s/%d%s" % ("pair" if pick_pair else "single", pick_bn,
+                               "/split%d" % pick_split if pick_split > 1 else ""),
         "picked_ms": picked_ms,
         "picked_tflops": flops / picked_ms / 1e9,
         "best": best,
@@ -119,7 +135,9 @@ def main(argv=None):
     a = ap.parse_args(argv)
     if not torch.cuda.is_available():
         sys.exit("tune: needs a CUDA device")
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda"),
+             torch.zeros(CLEAN_BYTES // 8, dtype=torch.int64, device="cuda"),
+             torch.empty((), dtype=torch.int64, device="cuda"))
     results = []
     for M, N, K in a.shapes:
         r = sweep_shape(M, N, K, a.reps, flush)

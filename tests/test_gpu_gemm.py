@@ -165,8 +165,8 @@ def test_tile_config_query(monkeypatch):
     """The planner's choice is a valid configuration, follows the A/B overrides, and the
     GEMM stays exact when launched with whatever it picked."""
     for M, N, K in [(4096, 4096, 4096), (128, 4096, 4096), (80666, 28672, 5376), (1, 8, 16)]:
-        bn, pair, resident = ck.ck_gemm_tile_config(M, N, K)
-        assert bn % 32 == 0 and 32 <= bn <= 256 and resident >= 1
+        bn, pair, resident, split = ck.ck_gemm_tile_config(M, N, K)
+        assert bn % 32 == 0 and 32 <= bn <= 256 and resident >= 1 and 1 <= split <= 8
         assert not pair or (M + 127) // 128 >= 2
     monkeypatch.setenv("CK_GEMM_BN", "96")
     monkeypatch.setenv("CK_GEMM_PAIR", "0")
@@ -174,3 +174,83 @@ def test_tile_config_query(monkeypatch):
     monkeypatch.setenv("CK_GEMM_PAIR", "1")
     assert ck.ck_gemm_tile_config(4096, 4096, 4096)[:2] == (96, True)
     assert ck.ck_gemm_tile_config(128, 4096, 4096)[:2] == (96, False)  # one tile row: no pair
+
+
+def run_s32(q, w, ws=None):
+    acc = ck.ck_int8_gemm_s32(q.to(DEV), w.to(DEV), ws=ws)
+    torch.cuda.synchronize()
+    assert ck.ck_device_error(clear=False) == 0
+    return acc.cpu().numpy()
+
+
+# shapes whose last partial wave is split along K: CTA pairs and single CTAs, K ranges
+# that do not divide evenly among the slices, one-slice-per-1024-K chunk boundaries
+@pytest.mark.parametrize("M,N,K,pair,split", [
+    (512, 1024, 2048, "1", "8"), (512, 1024, 2048, "1", "3"), (300, 712, 1104, "0", "4"), (300, 712, 1104, "1", "2"),
+    (4096, 2560, 1040, "1", "2"), (130, 264, 4160, "0", "7"), (1000, 520, 3088, "1", "5"),
+])
+def test_split_tail_exact(monkeypatch, M, N, K, pair, split):
+    """Units of the last partial wave computed as K-slices by different pairs / CTAs and
+    summed by the slice that arrives last: the int32 accumulators stay exact."""
+    monkeypatch.setenv("CK_GEMM_PAIR", pair)
+    monkeypatch.setenv("CK_GEMM_SPLIT", split)
+    assert ck.ck_gemm_tile_config(M, N, K)[3] == int(split)
+    q = synthetic.int8_uniform((M, K), seed=M + 3)
+    w = synthetic.int8_uniform((N, K), seed=N + 4)
+    ref = oracle.gemm_s32(q.numpy(), w.numpy())
+    for _ in range(2):  # the second launch finds the first one's arrival slots
+        got = run_s32(q, w)
+        bad = np.argwhere(got != ref)
+        assert bad.size == 0, "%d mismatches, first at %s" % (len(bad), bad[0])
+
+
+def test_split_tail_after_full_waves(monkeypatch):
+    """4096^3 with 256x256 pair tiles: three full waves, the last 28 tiles split in two
+    along K.  Exact on a row sample that includes the split tiles' rows (the last tile
+    rows of the grouped order)."""
+    monkeypatch.setenv("CK_GEMM_PAIR", "1")
+    monkeypatch.setenv("CK_GEMM_BN", "256")
+    monkeypatch.setenv("CK_GEMM_SPLIT", "2")
+    M, N, K = 4096, 4096, 4096
+    bn, pair, resident, split = ck.ck_gemm_tile_config(M, N, K)
+    assert (bn, pair) == (256, True) and (resident != 76 or split == 2)
+    q = synthetic.int8_uniform((M, K), seed=71)
+    w = synthetic.int8_uniform((N, K), seed=72)
+    got = run_s32(q, w)
+    rows = synthetic.sample_rows(M, n_random=48, seed=73)
+    ref = oracle.gemm_s32(q[rows].numpy(), w.numpy())
+    assert np.array_equal(got[rows], ref)
+
+
+def test_split_tail_ignores_stale_workspace(monkeypatch):
+    """The arrival slots are tagged per launch: a workspace full of random bytes (or of
+    an earlier launch's slots) changes nothing."""
+    monkeypatch.setenv("CK_GEMM_SPLIT", "4")
+    M, N, K = 512, 1024, 2048
+    assert ck.ck_gemm_tile_config(M, N, K)[3] == 4
+    q = synthetic.int8_uniform((M, K), seed=51)
+    w = synthetic.int8_uniform((N, K), seed=52)
+    ref = oracle.gemm_s32(q.numpy(), w.numpy())
+    nbytes = ck.load_library().ck_int8_gemm_workspace_size(M, N, K)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(53)
+    ws = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=DEV, generator=g)
+    assert np.array_equal(run_s32(q, w, ws=ws), ref)
+    assert np.array_equal(run_s32(q, w, ws=ws), ref)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_split_tail_dequant(monkeypatch, out_dtype):
+    """The fused epilogue after a K-split: within 1 ulp of the oracle, as without it."""
+    monkeypatch.setenv("CK_GEMM_SPLIT", "3")
+    M, N, K = 512, 1024, 2048
+    q = synthetic.int8_uniform((M, K), seed=61)
+    w = synthetic.int8_uniform((N, K), seed=62)
+    xs = synthetic.scale_uniform(M, seed=63, mul=0.02)
+    ws = synthetic.scale_uniform(N, seed=64, mul=0.01)
+    b = synthetic.normal_bf16((1, N), seed=65, std=0.5).reshape(N)
+    code = oracle.OUT_F32 if out_dtype == torch.float32 else oracle.OUT_BF16
+    ref = typed_reference(q, w, xs, ws, b, False, code)
+    y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert ulp_distance(out_bits(y), ref).max() <= MAX_ULP

@@ -129,7 +129,8 @@ def test_tile_config_query_validates_without_a_gpu(lib):
     import ctypes
     import int8_weight_quantized_gb300 as ck
     bn, pair = ctypes.c_int(), ctypes.c_int()
-    assert lib.ck_gemm_tile_config(16, 12, 32, ctypes.byref(bn), ctypes.byref(pair), None) == ck.CK_ERR_INVALID_ARG
-    st = lib.ck_gemm_tile_config(16, 16, 32, ctypes.byref(bn), ctypes.byref(pair), None)
+    assert lib.ck_gemm_tile_config(16, 12, 32, ctypes.byref(bn), ctypes.byref(pair), None, None) == \
+        ck.CK_ERR_INVALID_ARG
+    st = lib.ck_gemm_tile_config(16, 16, 32, ctypes.byref(bn), ctypes.byref(pair), None, None)
     if not torch.cuda.is_available():
         assert st in (ck.CK_ERR_CUDA, ck.CK_ERR_UNSUPPORTED_DEVICE)
