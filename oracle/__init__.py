@@ -46,6 +46,8 @@ def lib():
         L.ck_oracle_f32_to_bf16.restype = ctypes.c_uint16
         L.ck_oracle_prepare_convrot_weight.argtypes = [P, I64, I64, P, P]
         L.ck_oracle_prepare_convrot_weight.restype = ctypes.c_int
+        L.ck_oracle_w8a16_linear.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_int, P, P]
+        L.ck_oracle_w8a16_linear.restype = ctypes.c_int
         L.ck_oracle_num_threads.argtypes = []
         L.ck_oracle_num_threads.restype = ctypes.c_int
         _lib = L
@@ -208,3 +210,20 @@ def prepare_convrot_weight(W):
     if rc != 0:
         raise ValueError("oracle prepare_convrot_weight rejected the arguments (rc=%d)" % rc)
     return w, ws
+
+
+def w8a16_linear(x_bits, w, ws, bias_bits=None, mode=PER_ROW):
+    """16-bit-activation path: (y, mag), both float64 [M,N]; y before output rounding,
+    mag = |w_scale| * sum |a * w| (bounds any fp32 evaluation's rounding error)."""
+    x = _c(x_bits, np.uint16)
+    w = _c(w, np.int8)
+    ws = _c(ws, np.float32)
+    b = None if bias_bits is None else _c(bias_bits, np.uint16)
+    M, K = x.shape
+    N = w.shape[0]
+    y = np.empty((M, N), np.float64)
+    mag = np.empty((M, N), np.float64)
+    rc = lib().ck_oracle_w8a16_linear(_p(x), _p(w), _p(ws), _p(b), M, N, K, int(mode), _p(y), _p(mag))
+    if rc != 0:
+        raise ValueError("oracle w8a16_linear rejected the arguments (rc=%d)" % rc)
+    return y, mag

@@ -11,6 +11,9 @@
  *   q[m,k]   = clamp(rint(v[m,k] / x_scale[m]), -127, 127),  x_scale[m] = amax_k|v[m,k]| / 127
  *   v        = x                  (per-row / tensorwise modes)
  *   v        = x @ H              (ConvRot mode, H = blockdiag of normalized Sylvester H_128)
+ * and the 16-bit-activation path of the same layer (no activation quantize):
+ *   y[m,n] = w_scale[n] * sum_k a[m,k] * w[n,k] + bias[n],  a = x or bf16(x @ H)
+ * (ck_oracle_w8a16_linear, readings R12-R14 there).
  *
  *   - epilogue and its fp32 operation order: issue #280 "INT8 linears on sm_121 (GB10 /
  *     DGX Spark) run at ~37% of tensor-core peak ...", sections "Kernel used" and
@@ -364,6 +367,65 @@ int ck_oracle_prepare_convrot_weight(const float *W, int64_t N, int64_t K, int8_
             }
             free(v);
         }
+    }
+    return bad ? -1 : 0;
+}
+
+/* W8A16 linear: the 16-bit-activation path of issue #278 (section "Suggested fix":
+ * dequantize the INT8 weight on the fly and run the GEMM on 16-bit tensor cores; the
+ * stored weight keeps its INT8 footprint; for ConvRot the activation is rotated online,
+ * x_rot = x @ H, the GEMM runs in the rotated basis and the weight is not rotated back).
+ * Readings (also in the design notes):
+ *   R12 the activation is not quantized: a = x as given (bf16), or for ConvRot
+ *       a = bf16_rne(x @ H) with the fp32 block transform of R5 (16-bit tensor-core
+ *       operands hold bf16, so the rotated activation is rounded once);
+ *   R13 "dequantize on the fly" multiplies each code by w_scale[n]; this oracle keeps
+ *       the exact real-number result of that definition,
+ *           y[m,n] = w_scale[n] * sum_k a[m,k] * w[n,k] + bias[n],
+ *       which equals sum_k a[m,k] * (w[n,k] * w_scale[n]) + bias[n] exactly;
+ *   R14 tensorwise mode has one w_scale, per-row and ConvRot one per output row.
+ * The sum is taken in double: every product a*w is exact in double (8 + 7 significant
+ * bits) and K <= 131072 partial sums of magnitude < 2^53 ulps stay exact enough that
+ * the result is the real value to within 2^-50 relative of sum |a*w|.  The caller gets
+ * y (double, before any output rounding) and mag[m,n] = |w_scale[n]| * sum_k |a*w|,
+ * which bounds the rounding error of any fp32 evaluation of the same sum.
+ * x: bf16 bits [M,K]; w: int8 [N,K]; ws: fp32 [N] or [1]; bias: bf16 bits [N] or NULL.
+ * Returns 0, or -1 on a bad argument / allocation failure. */
+int ck_oracle_w8a16_linear(const uint16_t *x, const int8_t *w, const float *ws, const uint16_t *bias,
+                           int64_t M, int64_t N, int64_t K, int mode, double *y, double *mag)
+{
+    if (M < 0 || N < 0 || K <= 0 || mode < 0 || mode > 2 || (mode == 2 && K % 128 != 0))
+        return -1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        float *v = (float *)malloc((size_t)K * sizeof(float));
+        double *a = (double *)malloc((size_t)K * sizeof(double));
+        if (!v || !a) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t m = 0; m < M; m++) {
+                load_row(x, m, K, mode == 2, v);
+                for (int64_t k = 0; k < K; k++)
+                    a[k] = mode == 2 ? (double)bf16_bits_to_f32(f32_to_bf16_bits_rne(v[k])) : (double)v[k];
+                for (int64_t n = 0; n < N; n++) {
+                    double s = 0.0, sa = 0.0;
+                    for (int64_t k = 0; k < K; k++) {
+                        double p = a[k] * (double)w[n * K + k];
+                        s += p;
+                        sa += fabs(p);
+                    }
+                    double wsn = (double)(mode == 0 ? ws[0] : ws[n]);
+                    double b = bias ? (double)bf16_bits_to_f32(bias[n]) : 0.0;
+                    y[m * N + n] = wsn * s + b;
+                    mag[m * N + n] = fabs(wsn) * sa;
+                }
+            }
+        }
+        free(v);
+        free(a);
     }
     return bad ? -1 : 0;
 }

@@ -376,3 +376,108 @@ def test_linear_is_close_to_the_float_layer(mode):
     assert rel < 0.02  # the quantization error the pages call "~1 % against a bf16 reference"
     # and the composition is the GEMM of the quantized codes
     assert np.array_equal(out["acc"], out["q"].astype(np.int64) @ case.w.numpy().astype(np.int64).T)
+
+
+# ---- the 16-bit-activation path (issue #278, "Suggested fix") -----------------------
+
+def test_w8a16_brute_force_in_rationals():
+    """Tiny case summed in exact rational arithmetic from the definition
+    y = w_scale[n] * sum_k a[m,k] * w[n,k] + bias[n]."""
+    M, N, K = 3, 4, 32
+    x = synthetic.normal_bf16((M, K), seed=901)
+    w = synthetic.int8_uniform((N, K), seed=902).numpy()
+    ws = synthetic.scale_uniform(N, seed=903).numpy()
+    b = synthetic.normal_bf16((1, N), seed=904).reshape(N)
+    y, mag = oracle.w8a16_linear(bits(x), w, ws, bits(b), mode=oracle.PER_ROW)
+    xf = x.float().numpy()
+    bf = b.float().numpy()
+    for m in range(M):
+        for n in range(N):
+            s = sum(Fraction(float(xf[m, k])) * int(w[n, k]) for k in range(K))
+            exact = Fraction(float(ws[n])) * s + Fraction(float(bf[n]))
+            assert abs(Fraction(y[m, n]) - exact) <= Fraction(1, 2 ** 50) * (abs(exact) + 1)
+            ref_mag = Fraction(float(ws[n])) * sum(abs(Fraction(float(xf[m, k])) * int(w[n, k])) for k in range(K))
+            assert abs(Fraction(mag[m, n]) - ref_mag) <= Fraction(1, 2 ** 50) * (ref_mag + 1)
+
+
+def test_w8a16_one_hot_weights_select_activations():
+    """w[n] = c * e_{k_n}: y[m,n] = w_scale[n] * c * x[m,k_n] + bias[n], exactly."""
+    M, N, K = 5, 6, 48
+    x = synthetic.normal_bf16((M, K), seed=911)
+    ks = [3, 0, 47, 20, 11, 33]
+    cs = [1, -127, 127, 5, -2, 64]
+    w = np.zeros((N, K), np.int8)
+    for n, (k, c) in enumerate(zip(ks, cs)):
+        w[n, k] = c
+    ws = np.array([0.5, 0.25, 2.0, 1.0, 0.125, 4.0], np.float32)  # powers of two: exact
+    y, _ = oracle.w8a16_linear(bits(x), w, ws, None, mode=oracle.PER_ROW)
+    xf = x.float().numpy().astype(np.float64)
+    for n, (k, c) in enumerate(zip(ks, cs)):
+        assert np.array_equal(y[:, n], float(ws[n]) * c * xf[:, k])
+
+
+def test_w8a16_tensorwise_uses_the_single_scale():
+    M, N, K = 4, 8, 64
+    x = synthetic.normal_bf16((M, K), seed=921)
+    w = synthetic.int8_uniform((N, K), seed=922).numpy()
+    y1, m1 = oracle.w8a16_linear(bits(x), w, np.array([0.01], np.float32), None, mode=oracle.TENSORWISE)
+    y2, m2 = oracle.w8a16_linear(bits(x), w, np.full((N,), 0.01, np.float32), None, mode=oracle.PER_ROW)
+    assert np.array_equal(y1, y2) and np.array_equal(m1, m2)
+
+
+def test_w8a16_agrees_with_the_int8_path_when_quantization_is_lossless():
+    """Rows that are integers times 2^e with |max| = 127 * 2^e quantize without loss
+    (x_scale = 2^e, q = x / 2^e), so the INT8 layer and the 16-bit path compute the
+    same real number: the INT8 epilogue rounds it in fp32 and then to bf16, the
+    16-bit value rounded to bf16 must be within one bf16 step of it."""
+    M, N, K = 8, 16, 256
+    g = np.random.default_rng(931)
+    q = g.integers(-127, 128, size=(M, K))
+    q[:, 0] = 127
+    e = g.integers(-6, 4, size=(M, 1))
+    xv = (q * (2.0 ** e)).astype(np.float32)
+    x = torch.tensor(xv).to(torch.bfloat16)
+    assert torch.equal(x.float(), torch.tensor(xv))  # all exact in bf16
+    w = synthetic.int8_uniform((N, K), seed=932).numpy()
+    ws = synthetic.scale_uniform(N, seed=933).numpy()
+    b = synthetic.normal_bf16((1, N), seed=934).reshape(N)
+    r8 = oracle.int8_linear(bits(x), w, ws, bits(b), mode=oracle.PER_ROW)
+    assert np.array_equal(r8["xs"], (2.0 ** e[:, 0]).astype(np.float32))
+    y16, _ = oracle.w8a16_linear(bits(x), w, ws, bits(b), mode=oracle.PER_ROW)
+    y16_bits = oracle.f32_to_bf16(y16.astype(np.float32))
+    d = np.abs(oracle.bf16_to_f32(y16_bits).astype(np.float64) - oracle.bf16_to_f32(r8["y"]).astype(np.float64))
+    step = np.abs(oracle.bf16_to_f32(r8["y"]).astype(np.float64)) * 2.0 ** -7 + 1e-30
+    assert np.all(d <= step)
+
+
+def test_w8a16_convrot_rounds_the_rotated_activation_once():
+    """x rows = c * e_j (c a power of two): x @ H = c * H[j] / sqrt(128), whose fp32
+    values are +-c * 0x3DB504F3, rounded to bf16 0x3DB5.  With an all-ones weight row,
+    y = w_scale * c * bf16(1/sqrt(128)) * sum_k H[j,k] = 128 * (...) for j = 0, else 0."""
+    K = 128
+    rows = [0, 1, 5, 127]
+    c = 4.0
+    xv = np.zeros((len(rows), K), np.float32)
+    for i, j in enumerate(rows):
+        xv[i, j] = c
+    x = torch.tensor(xv).to(torch.bfloat16)
+    w = np.ones((2, K), np.int8)
+    ws = np.array([1.0, 0.5], np.float32)
+    y, mag = oracle.w8a16_linear(bits(x), w, ws, None, mode=oracle.CONVROT)
+    h = float(oracle.bf16_to_f32(np.array([0x3DB5], np.uint16))[0])
+    for i, j in enumerate(rows):
+        expect = c * h * (128 if j == 0 else 0)
+        assert y[i, 0] == expect and y[i, 1] == 0.5 * expect
+        assert mag[i, 0] == c * h * 128
+
+
+def test_w8a16_convrot_approximates_the_float_layer():
+    """The rotated-basis layer with an INT8 weight approximates x @ W^T (the only loss
+    is the weight's quantization and one bf16 rounding of x @ H)."""
+    M, N, K = 16, 64, 512
+    x = synthetic.normal_bf16((M, K), seed=941)
+    W = synthetic.normal_f32((N, K), seed=942, std=0.02).numpy()
+    w, ws = oracle.prepare_convrot_weight(W)
+    y, _ = oracle.w8a16_linear(bits(x), w, ws, None, mode=oracle.CONVROT)
+    ref = x.float().numpy().astype(np.float64) @ W.astype(np.float64).T
+    assert np.linalg.norm(y - ref) / np.linalg.norm(ref) < 0.01
