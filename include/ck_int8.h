@@ -141,6 +141,24 @@ int ck_int8_linear(const void *x, const int8_t *w, const float *w_scale, const v
  * The result is the w / w_scale that ck_int8_linear takes in CK_CONVROT mode. */
 int ck_convrot_prepare_weight(const float *W, int64_t N, int64_t K, int8_t *w, float *w_scale, void *stream);
 
+/* The 16-bit-activation path of the same layer (issue #278, "Suggested fix": the INT8
+ * weight dequantized on the fly, the GEMM on 16-bit tensor cores, the weight keeping its
+ * INT8 footprint; for ConvRot the activation rotated online and the weight used as
+ * stored, in the rotated basis).  No activation quantize:
+ *   y[m,n] = out( fp32( sum_k a[m,k] * w[n,k] ) * w_scale[n] + bias[n] )
+ *   a = x (CK_TENSORWISE, CK_PER_ROW) or bf16_rne(x @ H) (CK_CONVROT, K % 128 == 0; the
+ *   fp32 block transform of ck_quantize_int8_rowwise, rounded once).
+ * The codes are exact in bf16; the sum over all of K is accumulated in fp32 by the tensor
+ * cores (rounding order not specified: error at most about K * 2^-24 * sum_k |a w|),
+ * then scaled, biased and rounded to out_dtype like ck_int8_linear's epilogue.
+ *   x, w, w_scale (fp32 [1] for CK_TENSORWISE, else [N]), bias, y, out_dtype: as for
+ *   ck_int8_linear.  workspace: ck_w8a16_linear_workspace_size() bytes (the widened
+ *   weight, and the rotated activation for ConvRot). */
+size_t ck_w8a16_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
+int ck_w8a16_linear(const void *x, const int8_t *w, const float *w_scale, const void *bias, void *y, int64_t M,
+                    int64_t N, int64_t K, int mode, int out_dtype, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
 /* GEMM + fused dequant on an already-quantized activation (the second half of
  * ck_int8_linear): q int8 [M,K], x_scale fp32 [M] (or [1] if scalar_scales), w int8
  * [N,K], w_scale fp32 [N] (or [1]), bias bf16 [N] or NULL, y [M,N] of out_dtype

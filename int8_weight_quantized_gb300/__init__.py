@@ -52,6 +52,8 @@ def load_library(path=None):
         "ck_int8_linear": ([P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_convrot_prepare_weight": ([P, I64, I64, P, P, P], I),
         "ck_int8_gemm_workspace_size": ([I64, I64, I64], SZ),
+        "ck_w8a16_linear_workspace_size": ([I64, I64, I64, I], SZ),
+        "ck_w8a16_linear": ([P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_int8_gemm_dequant": ([P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_int8_gemm_s32": ([P, P, P, I64, I64, I64, P, SZ, P], I),
         "ck_profile_begin": ([I], I),
@@ -177,6 +179,26 @@ def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stre
     ws = workspace(need, x.device) if ws is None else ws
     _check(L.ck_int8_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, int(mode), code,
                             _ptr(ws), ws.numel(), _stream(stream)))
+    return y
+
+
+def ck_w8a16_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stream=None, out_dtype=torch.bfloat16):
+    """y [M,N] of out_dtype = (bf16 x [@ H]) . (int8 w)^T summed in fp32, * w_scale (+ bias)."""
+    code = _out_code(out_dtype)
+    M, K = x.shape
+    N = w.shape[0]
+    _req(x, torch.bfloat16, (M, K), "x")
+    _req(w, torch.int8, (N, K), "w")
+    _req(w_scale, torch.float32, (1,) if mode == TENSORWISE else (N,), "w_scale")
+    if bias is not None:
+        _req(bias, torch.bfloat16, (N,), "bias")
+    y = torch.empty((M, N), dtype=out_dtype, device=x.device) if y is None else y
+    _req(y, out_dtype, (M, N), "y")
+    L = load_library()
+    need = L.ck_w8a16_linear_workspace_size(M, N, K, int(mode))
+    ws = workspace(need, x.device) if ws is None else ws
+    _check(L.ck_w8a16_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, int(mode), code,
+                             _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 

@@ -380,6 +380,85 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
     return CK_OK;
 }
 
+// ---- the 16-bit-activation path --------------------------------------------------
+static size_t w8a16_ws_bytes(int64_t M, int64_t N, int64_t K, int mode)
+{
+    return align_up((size_t)N * K * 2) + (mode == CK_CONVROT ? align_up((size_t)M * K * 2) : 0);
+}
+
+size_t ck_w8a16_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return 0;
+    return w8a16_ws_bytes(M, N, K, mode);
+}
+
+int ck_w8a16_linear(const void* x, const int8_t* w, const float* w_scale, const void* bias, void* y, int64_t M,
+                    int64_t N, int64_t K, int mode, int out_dtype, void* workspace, size_t workspace_bytes,
+                    void* stream)
+{
+    if (mode != CK_TENSORWISE && mode != CK_PER_ROW && mode != CK_CONVROT)
+        return fail(CK_ERR_INVALID_ARG, "mode must be 0 (tensorwise), 1 (per-row) or 2 (ConvRot), got %d", mode);
+    if (!valid_out_dtype(out_dtype))
+        return fail(CK_ERR_INVALID_ARG, "out_dtype must be 0 (bf16), 1 (fp16) or 2 (fp32), got %d", out_dtype);
+    int st = check_gemm_shape(M, N, K);
+    if (st != CK_OK)
+        return st;
+    if (mode == CK_CONVROT && K % 128 != 0)
+        return fail(CK_ERR_INVALID_ARG, "ConvRot needs K % 128 == 0 (got %lld)", (long long)K);
+    if (M == 0)
+        return CK_OK;  // empty batch: x and y may be NULL
+    CK_REQUIRE_PTR(x);
+    CK_REQUIRE_PTR(w);
+    CK_REQUIRE_PTR(w_scale);
+    CK_REQUIRE_PTR(y);
+    CK_REQUIRE_PTR(workspace);
+    if (bias != nullptr && !aligned16(bias))
+        return fail(CK_ERR_INVALID_ARG, "bias must be 16-byte aligned");
+    const size_t need = w8a16_ws_bytes(M, N, K, mode);
+    if (workspace_bytes < need)
+        return fail(CK_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+    DeviceInfo dev;
+    if ((st = check_device(&dev)) != CK_OK)
+        return st;
+    log_shape("w8a16_linear", M, N, K, mode, "widen (+ rotate) + tcgen05 bf16 GEMM, fp32 sum over K");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* p8 = static_cast<uint8_t*>(workspace);
+    void* b16 = p8;
+    void* a16 = p8 + align_up((size_t)N * K * 2);
+    cudaError_t e;
+    if (mode == CK_CONVROT) {
+        ProfScope ps(kProfQuantize, 1, s);
+        e = launch_rotate_bf16(x, M, K, a16, w, N * K, b16, dev, s);
+    } else {
+        ProfScope ps(kProfWiden, 1, s);
+        e = launch_widen_int8(w, b16, N * K, dev, s);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "w8a16_linear operand launch");
+    GemmProblem p;
+    p.a = mode == CK_CONVROT ? a16 : x;
+    p.b = b16;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.x_scale = nullptr;
+    p.w_scale = w_scale;
+    p.bias = bias;
+    p.scalar_scales = mode == CK_TENSORWISE;
+    p.y = y;
+    p.out_dtype = out_dtype;
+    p.mixed = true;
+    std::string why;
+    {
+        ProfScope ps(kProfGemm, 1, s);
+        e = launch_gemm(p, dev, s, &why);
+    }
+    if (e != cudaSuccess)
+        return why.empty() ? cuda_fail(e, "w8a16_linear GEMM launch") : fail(CK_ERR_CUDA, "%s", why.c_str());
+    return CK_OK;
+}
+
 int ck_convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8_t* w, float* w_scale, void* stream)
 {
     if (N < 0 || K <= 0)
@@ -544,7 +623,7 @@ int ck_gemm_tile_config(int64_t M, int64_t N, int64_t K, int* bn, int* cta_pair,
     if ((st = check_device(&dev)) != CK_OK)
         return st;
     GemmPlan plan;
-    cudaError_t e = plan_gemm(std::max<int64_t>(M, 1), N, K, dev, &plan);
+    cudaError_t e = plan_gemm(std::max<int64_t>(M, 1), N, K, false, dev, &plan);
     if (e != cudaSuccess)
         return cuda_fail(e, "GEMM planning");
     *bn = plan.bn;

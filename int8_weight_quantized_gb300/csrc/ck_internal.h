@@ -46,6 +46,7 @@ struct GemmProblem {
     void* y = nullptr;           // [M,N] of the output type
     int out_dtype = 0;           // 0 bf16, 1 fp16, 2 fp32
     void* tail = nullptr;        // gemm_tail_bytes(M, N) bytes of workspace (K-split tail)
+    bool mixed = false;          // a = 16-bit activations, fp32 sum over all of K, no x_scale
     int32_t* acc = nullptr;      // int32 [M,N]
 };
 
@@ -88,7 +89,7 @@ struct GemmPlan {
     int64_t full_units = 0;  // units computed whole; the rest are split
     int split = 1;
 };
-cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev, GemmPlan* plan);
+cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, bool mixed, const DeviceInfo& dev, GemmPlan* plan);
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why);
 cudaError_t launch_quantize_rows(const void* x, int64_t M, int64_t K, bool rotate, int8_t* q8, void* q16,
                                  float* x_scale, const DeviceInfo& dev, cudaStream_t s);
@@ -113,6 +114,10 @@ size_t prep_tensorwise_scratch_bytes(int max_blocks);
 cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q16, float* x_scale, void* scratch,
                                    int max_blocks, const int8_t* w8, int64_t w_n, void* w16, const DeviceInfo& dev,
                                    cudaStream_t s);
+// 16-bit-activation ConvRot operand: a16 = bf16(x @ H) ([M,K], K % 128 == 0), plus the
+// int8 -> bf16 weight widening, in one launch.
+cudaError_t launch_rotate_bf16(const void* x, int64_t M, int64_t K, void* a16, const int8_t* w8, int64_t w_n,
+                               void* w16, const DeviceInfo& dev, cudaStream_t s);
 // Two int8 -> bf16 widenings in one launch.
 cudaError_t launch_widen2(const int8_t* a8, int64_t a_n, void* a16, const int8_t* b8, int64_t b_n, void* b16,
                           const DeviceInfo& dev, cudaStream_t s);

@@ -111,6 +111,7 @@ struct Args {
     uint32_t tx_bytes;      // bytes of one k-block counted on the (leader's) full barrier
     int units_m, tiles_m, tiles_n, num_kb, group_m;
     int scalar_scales;
+    int chunk_kb;           // k-blocks per TMEM accumulation: CHUNK_KB (exact), all of K (16-bit activations)
     uint64_t timeout_ns;
     // K-split of the last partial wave: units [full_units, num_units) are each computed
     // as `split` K-slices by different units of the grid; every slice writes its int32
@@ -230,7 +231,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 // hold 16K registers each: at most 168 registers per thread at launch, re-balanced to
 // REGS_WG0 / REGS_EPI once the roles split (32 x (56 + 2 x 216) <= 16K per
 // sub-partition as well).
-template <bool RAW, bool PAIR, int OUT>
+// MIXED: 16-bit activations times int8 weight codes (both bf16 operands), the fp32
+// accumulation over all of K kept in TMEM, epilogue (sum * w_scale) + bias.
+template <bool RAW, bool PAIR, int OUT, bool MIXED>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const Args args)
@@ -359,7 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 bool ok = true;
                 for (int64_t it = cluster; ok && it < args.num_items; it += clusters) {
                     const Item w = item_of(it, args);
-                    for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += CHUNK_KB) {
+                    for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += args.chunk_kb) {
                         const uint32_t buf = acc_iter & 1u;
                         const uint32_t acc_phase = (acc_iter >> 1) & 1u;
                         if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort_flag, err, kErrWaitMma, args.timeout_ns)) {
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                         tc_fence_after();
                         const uint32_t d_tmem = tmem_base + buf * BN;
-                        const int kend = min(kb0 + CHUNK_KB, w.kb_end);
+                        const int kend = min(kb0 + args.chunk_kb, w.kb_end);
                         for (int kb = kb0; kb < kend; ++kb) {
                             if (!mbar_wait(&full[stage], phase, abort_flag, err, kErrWaitMma, args.timeout_ns)) {
                                 ok = false;
@@ -437,18 +440,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int64_t cbase = n0 + half * 128;
             float xsv = 0.0f, ws_scalar = 0.0f;
             if (!RAW) {  // the scalar scales and this lane's row scale, in flight during the K loop
-                if (args.scalar_scales) {
+                if (args.scalar_scales)
                     ws_scalar = __ldg(args.ws);
-                    xsv = __ldg(args.xs);
-                } else if (row < args.M) {
-                    xsv = __ldg(args.xs + row);
-                }
+                if (!MIXED)
+                    xsv = args.scalar_scales ? __ldg(args.xs) : (row < args.M ? __ldg(args.xs + row) : 0.0f);
             }
             int32_t run[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j)
                 run[j] = 0;
-            for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += CHUNK_KB) {
+            for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += args.chunk_kb) {
                 const uint32_t buf = acc_iter & 1u;
                 const uint32_t acc_phase = (acc_iter >> 1) & 1u;
                 // one lane polls, the warp follows its verdict (keeps the warp converged
@@ -471,7 +472,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            run[g * 16 + j] += __float2int_rz(__uint_as_float(v[j]));  // exact integer
+                            if (MIXED)  // one chunk holds the whole fp32 sum: keep its bits
+                                run[g * 16 + j] = (int32_t)v[j];
+                            else
+                                run[g * 16 + j] += __float2int_rz(__uint_as_float(v[j]));  // exact integer
                     }
                 }
                 tc_fence_before();
@@ -591,8 +595,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         float t[PC];
 #pragma unroll
                         for (int i = 0; i < PC; ++i) {
-                            t[i] = __int2float_rn(run[j0 + i]);
-                            t[i] = __fmul_rn(t[i], xsv);
+                            if (MIXED) {  // 16-bit activations: (sum * w_scale) + bias
+                                t[i] = __int_as_float(run[j0 + i]);
+                            } else {
+                                t[i] = __int2float_rn(run[j0 + i]);
+                                t[i] = __fmul_rn(t[i], xsv);
+                            }
                             t[i] = __fmul_rn(t[i], wsv[i]);
                             if (args.bias)
                                 t[i] = __fadd_rn(t[i], bv[i]);
@@ -706,7 +714,7 @@ static bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ba
     return true;
 }
 
-template <bool RAW, bool PAIR, int OUT>
+template <bool RAW, bool PAIR, int OUT, bool MIXED>
 static cudaError_t ensure_smem_attr(int device)
 {
     static bool done[64] = {};
@@ -714,7 +722,7 @@ static cudaError_t ensure_smem_attr(int device)
     std::lock_guard<std::mutex> lock(mu);
     if (device >= 0 && device < 64 && done[device])
         return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR, OUT>,
+    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR, OUT, MIXED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)gemm::Mode<PAIR>::SMEM_BYTES);
     if (e == cudaSuccess) {
@@ -722,7 +730,7 @@ static cudaError_t ensure_smem_attr(int device)
         // with (registers are granted per warp in units of 8 per thread), else the
         // epilogue's increase would wait forever: refuse to launch instead
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<RAW, PAIR, OUT>);
+        e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<RAW, PAIR, OUT, MIXED>);
         if (e == cudaSuccess &&
             (uint64_t)((fa.numRegs + 7) / 8 * 8) * gemm::THREADS < (uint64_t)gemm::REGS_NEEDED_PER_BLOCK)
             e = cudaErrorInvalidConfiguration;
@@ -763,13 +771,13 @@ static cudaError_t resident_units(const DeviceInfo& dev, int64_t* out)
     std::lock_guard<std::mutex> lock(mu);
     int& n = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
     if (n == 0) {
-        cudaError_t e = ensure_smem_attr<false, true, gemm::kOutBf16>(dev.device);
+        cudaError_t e = ensure_smem_attr<false, true, gemm::kOutBf16, false>(dev.device);
         if (e != cudaSuccess)
             return e;
         cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = make_config(true, gemm::Mode<true>::SMEM_BYTES, nullptr, attr);
         cfg.gridDim = dim3(2 * (dev.sm_count / 2));
-        e = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_kernel<false, true, gemm::kOutBf16>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_kernel<false, true, gemm::kOutBf16, false>, &cfg);
         if (e != cudaSuccess)
             return e;
         if (n <= 0)
@@ -833,7 +841,8 @@ static TileCost tile_cost(bool pair, int bn, int64_t units, int64_t resident, in
 // CK_GEMM_SPLIT=1 turns the K-split tail off and CK_GEMM_SPLIT=<s> asks for s slices
 // where the tail allows it (A/B timing).
 static void choose_tile(int64_t M, int64_t N, int num_kb, int64_t tiles_m, int64_t resident_pair,
-                        int64_t resident_single, bool pair_allowed, bool single_allowed, GemmPlan* plan)
+                        int64_t resident_single, bool pair_allowed, bool single_allowed, bool no_split,
+                        GemmPlan* plan)
 {
     int force_bn = 0, force_split = 0;
     if (const char* f = std::getenv("CK_GEMM_BN")) {
@@ -846,6 +855,8 @@ static void choose_tile(int64_t M, int64_t N, int num_kb, int64_t tiles_m, int64
         if (v >= 1 && v <= kTailMaxSplit)
             force_split = v;
     }
+    if (no_split)
+        force_split = 1;
     const int64_t tail_ctas = gemm_tail_ctas(M, N);
     int64_t best_cost = -1;
     bool best_forced = false;  // the best so far has the requested split
@@ -877,12 +888,12 @@ static void choose_tile(int64_t M, int64_t N, int num_kb, int64_t tiles_m, int64
 
 // Launch with programmatic stream serialization and, for pairs, 2-CTA clusters; the
 // persistent grid is as many units as can be resident at once.
-template <bool RAW, bool PAIR, int OUT>
+template <bool RAW, bool PAIR, int OUT, bool MIXED>
 static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                                  const gemm::Args& a, const DeviceInfo& dev, cudaStream_t s)
 {
     using namespace gemm;
-    cudaError_t e = ensure_smem_attr<RAW, PAIR, OUT>(dev.device);
+    cudaError_t e = ensure_smem_attr<RAW, PAIR, OUT, MIXED>(dev.device);
     if (e != cudaSuccess)
         return e;
     int64_t resident = 0;
@@ -892,7 +903,7 @@ static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB,
     cudaLaunchConfig_t cfg = make_config(PAIR, Mode<PAIR>::SMEM_BYTES, s, attr);
     const int64_t units = std::min<int64_t>(a.num_items, resident);
     cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units));
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR, OUT>, tmA, tmB, tmY, a);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR, OUT, MIXED>, tmA, tmB, tmY, a);
 }
 
 // A 64-bit tag no earlier launch of this process used (high-entropy start, so slots
@@ -913,7 +924,7 @@ static unsigned long long next_gemm_epoch()
     return e;
 }
 
-cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev, GemmPlan* plan)
+cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, bool mixed, const DeviceInfo& dev, GemmPlan* plan)
 {
     const int64_t tiles_m = (M + gemm::BM - 1) / gemm::BM;
     // CK_GEMM_PAIR=0 / =1 restricts the choice to single CTAs / CTA pairs (A/B timing);
@@ -928,8 +939,29 @@ cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev, Ge
     if (e != cudaSuccess)
         return e;
     const int num_kb = (int)((K + gemm::BK - 1) / gemm::BK);
-    choose_tile(M, N, num_kb, tiles_m, resident_pair, resident_single, pair_allowed, single_allowed, plan);
+    // the 16-bit-activation kernels keep one fp32 sum per tile: no K-split
+    choose_tile(M, N, num_kb, tiles_m, resident_pair, resident_single, pair_allowed, single_allowed, mixed, plan);
     return cudaSuccess;
+}
+
+// The dequant kernels by output type and tile mode.
+template <bool MIXED>
+static cudaError_t launch_dequant(bool pair, int out_dtype, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                  const CUtensorMap& tmY, const gemm::Args& a, const DeviceInfo& dev,
+                                  cudaStream_t s)
+{
+    using namespace gemm;
+    switch (out_dtype) {
+    case kOutF16:
+        return pair ? launch_kernel<false, true, kOutF16, MIXED>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutF16, MIXED>(tmA, tmB, tmY, a, dev, s);
+    case kOutF32:
+        return pair ? launch_kernel<false, true, kOutF32, MIXED>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutF32, MIXED>(tmA, tmB, tmY, a, dev, s);
+    default:
+        return pair ? launch_kernel<false, true, kOutBf16, MIXED>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutBf16, MIXED>(tmA, tmB, tmY, a, dev, s);
+    }
 }
 
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why)
@@ -967,9 +999,10 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.tiles_m = (int)((p.M + BM - 1) / BM);
     a.num_kb = (int)((p.K + BK - 1) / BK);
     a.scalar_scales = p.scalar_scales;
+    a.chunk_kb = p.mixed ? a.num_kb : CHUNK_KB;
     a.timeout_ns = DEFAULT_TIMEOUT_NS;
     GemmPlan plan;
-    const cudaError_t e = plan_gemm(p.M, p.N, p.K, dev, &plan);
+    const cudaError_t e = plan_gemm(p.M, p.N, p.K, p.mixed, dev, &plan);
     if (e != cudaSuccess)
         return e;
     const bool pair = plan.pair;
@@ -1000,19 +1033,11 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
         return cudaErrorInvalidValue;
     if (raw)
-        return pair ? launch_kernel<true, true, kOutBf16>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<true, false, kOutBf16>(tmA, tmB, tmY, a, dev, s);
-    switch (p.out_dtype) {
-    case kOutF16:
-        return pair ? launch_kernel<false, true, kOutF16>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<false, false, kOutF16>(tmA, tmB, tmY, a, dev, s);
-    case kOutF32:
-        return pair ? launch_kernel<false, true, kOutF32>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<false, false, kOutF32>(tmA, tmB, tmY, a, dev, s);
-    default:
-        return pair ? launch_kernel<false, true, kOutBf16>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<false, false, kOutBf16>(tmA, tmB, tmY, a, dev, s);
-    }
+        return pair ? launch_kernel<true, true, kOutBf16, false>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<true, false, kOutBf16, false>(tmA, tmB, tmY, a, dev, s);
+    if (p.mixed)
+        return launch_dequant<true>(pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
+    return launch_dequant<false>(pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
 }
 
 cudaError_t read_device_error(unsigned int* value, bool clear)

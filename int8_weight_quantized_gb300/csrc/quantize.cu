@@ -698,6 +698,40 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
     }
 }
 
+// The 16-bit-activation ConvRot operand: x @ H (the same fp32 block transform as the
+// quantizing path), rounded once to bf16.  The 128-blocks of the flattened x are
+// independent (K % 128 == 0, so no block spans two rows): a warp takes 32 consecutive
+// 16-byte vectors, two blocks, at a time.  The launch also widens the weight.
+__global__ void __launch_bounds__(256) rotate_bf16_kernel(const uint4* __restrict__ x, int64_t nvec,
+                                                          uint4* __restrict__ out, const uint4* __restrict__ w8,
+                                                          int64_t w_n16, uint4* __restrict__ w16)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32; base < nvec;
+         base += warps * 32) {
+        const int64_t i = base + lane;
+        // a warp's 32 vectors are two whole blocks or, at the very end, the last block
+        // (lanes 16-31 then idle: their shuffle partners stay within lanes 16-31)
+        const uint4 raw = i < nvec ? ld_stream(x + i) : make_uint4(0, 0, 0, 0);
+        float v[8];
+        unpack8(raw, v);
+        fwht_slot(v, lane);
+        if (i < nvec) {
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                o[e] = *reinterpret_cast<uint32_t*>(&b);
+            }
+            out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    widen_share(w8, w_n16, w16);
+}
+
 // Two int8 -> bf16 widenings in one launch (operands of the pre-quantized GEMM entries).
 __global__ void __launch_bounds__(256) widen2_kernel(const uint4* __restrict__ a8, int64_t a_n16,
                                                      uint4* __restrict__ a16, const uint4* __restrict__ b8,
@@ -916,6 +950,17 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
                       static_cast<quant::EpochSlot*>(scratch), next_prep_epoch(), static_cast<__nv_bfloat16*>(q16),
                       x_scale, reinterpret_cast<const uint4*>(w8), w_n >> 4, static_cast<uint4*>(w16),
                       (uint64_t)2000000000ull, err);
+}
+
+cudaError_t launch_rotate_bf16(const void* x, int64_t M, int64_t K, void* a16, const int8_t* w8, int64_t w_n,
+                               void* w16, const DeviceInfo& dev, cudaStream_t s)
+{
+    const int64_t nvec = (M * K) >> 3;
+    const int64_t want = std::max<int64_t>(1, (nvec + 255) / 256);  // 8 warps x 32 vectors per block
+    const int grid = (int)std::min<int64_t>(want, (int64_t)8 * dev.sm_count);
+    return launch_pdl(quant::rotate_bf16_kernel, grid, 256, 0, s, static_cast<const uint4*>(x), nvec,
+                      static_cast<uint4*>(a16), reinterpret_cast<const uint4*>(w8), w_n >> 4,
+                      static_cast<uint4*>(w16));
 }
 
 cudaError_t launch_widen2(const int8_t* a8, int64_t a_n, void* a16, const int8_t* b8, int64_t b_n, void* b16,
