@@ -48,6 +48,8 @@ def lib():
         L.ck_oracle_prepare_convrot_weight.restype = ctypes.c_int
         L.ck_oracle_w8a16_linear.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_int, P, P]
         L.ck_oracle_w8a16_linear.restype = ctypes.c_int
+        L.ck_oracle_dequant_residual.argtypes = [P, P, P, P, P, ctypes.c_int, I64, I64, ctypes.c_int, P]
+        L.ck_oracle_dequant_residual.restype = None
         L.ck_oracle_num_threads.argtypes = []
         L.ck_oracle_num_threads.restype = ctypes.c_int
         _lib = L
@@ -176,6 +178,21 @@ def dequant_typed(acc, xs, ws, bias_bits=None, scalar_scales=False, out_dtype=OU
     y = np.empty((M, N), np.float32 if out_dtype == OUT_F32 else np.uint16)
     lib().ck_oracle_dequant_typed(_p(acc), _p(xs), _p(ws), _p(b), int(bool(scalar_scales)), M, N, int(out_dtype),
                                   _p(y))
+    return y
+
+
+def dequant_residual(acc, xs, ws, residual, bias_bits=None, scalar_scales=False, out_dtype=OUT_BF16):
+    """Epilogue with a residual: residual is float32 [M,N] (values of the output-type
+    tensor, converted exactly); returns bf16 / fp16 bits or fp32 values [M,N]."""
+    acc = _c(acc, np.int32)
+    xs = _c(xs, np.float32)
+    ws = _c(ws, np.float32)
+    r = _c(residual, np.float32)
+    b = None if bias_bits is None else _c(bias_bits, np.uint16)
+    M, N = acc.shape
+    y = np.empty((M, N), np.float32 if out_dtype == OUT_F32 else np.uint16)
+    lib().ck_oracle_dequant_residual(_p(acc), _p(xs), _p(ws), _p(b), _p(r), int(bool(scalar_scales)), M, N,
+                                     int(out_dtype), _p(y))
     return y
 
 

@@ -299,6 +299,35 @@ void ck_oracle_dequant_typed(const int32_t *acc, const float *xs, const float *w
     }
 }
 
+/* The epilogue with a residual added (issue #280, section "Kernel used", mentions
+ * residual-fused calls of the dequant GEMM).  Reading R15: the residual r[m,n] is given
+ * in the output type and added in fp32 after the bias, one more separately rounded
+ * operation:  y = out((((float(acc) * xs) * ws) + bias) + r).  r holds fp32 values (the
+ * caller converts its bf16 / fp16 / fp32 tensor exactly). */
+void ck_oracle_dequant_residual(const int32_t *acc, const float *xs, const float *ws, const uint16_t *bias,
+                                const float *r, int scalar_scales, int64_t M, int64_t N, int out_dtype, void *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++) {
+        float xsm = scalar_scales ? xs[0] : xs[m];
+        for (int64_t n = 0; n < N; n++) {
+            float wsn = scalar_scales ? ws[0] : ws[n];
+            float t = (float)acc[m * N + n];
+            t = t * xsm;
+            t = t * wsn;
+            if (bias)
+                t = t + bf16_bits_to_f32(bias[n]);
+            t = t + r[m * N + n];
+            if (out_dtype == 2)
+                ((float *)y)[m * N + n] = t;
+            else if (out_dtype == 1)
+                ((uint16_t *)y)[m * N + n] = f32_to_f16_bits_rne(t);
+            else
+                ((uint16_t *)y)[m * N + n] = f32_to_bf16_bits_rne(t);
+        }
+    }
+}
+
 /* The whole linear layer in one call.  mode: 0 tensorwise, 1 per-row, 2 ConvRot
  * (for ConvRot, w is the pre-rotated, pre-quantized W_rot and is used as is).
  * Optional outputs q_out [M,K], xs_out [M] (or [1]) and acc_out [M,N] may be NULL.

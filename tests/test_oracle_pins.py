@@ -481,3 +481,58 @@ def test_w8a16_convrot_approximates_the_float_layer():
     y, _ = oracle.w8a16_linear(bits(x), w, ws, None, mode=oracle.CONVROT)
     ref = x.float().numpy().astype(np.float64) @ W.astype(np.float64).T
     assert np.linalg.norm(y - ref) / np.linalg.norm(ref) < 0.01
+
+
+# ---- residual-fused epilogue ---------------------------------------------------------
+
+@pytest.mark.parametrize("out_dtype", [oracle.OUT_BF16, oracle.OUT_F16, oracle.OUT_F32])
+def test_residual_zero_is_the_plain_epilogue(out_dtype):
+    M, N = 16, 24
+    g = np.random.default_rng(951)
+    acc = g.integers(-2 ** 20, 2 ** 20, size=(M, N)).astype(np.int32)
+    xs = synthetic.scale_uniform(M, seed=952, mul=0.02).numpy()
+    ws = synthetic.scale_uniform(N, seed=953, mul=0.01).numpy()
+    b = bits(synthetic.normal_bf16((1, N), seed=954).reshape(N))
+    plain = oracle.dequant_typed(acc, xs, ws, b, out_dtype=out_dtype)
+    with_r = oracle.dequant_residual(acc, xs, ws, np.zeros((M, N), np.float32), b, out_dtype=out_dtype)
+    assert np.array_equal(plain.view(np.uint8), with_r.view(np.uint8))
+
+
+def test_residual_cancelling_the_layer_gives_zero():
+    """r = -(the fp32 layer value): the last addition is exact and gives 0."""
+    M, N = 8, 16
+    g = np.random.default_rng(961)
+    acc = g.integers(-2 ** 20, 2 ** 20, size=(M, N)).astype(np.int32)
+    xs = synthetic.scale_uniform(M, seed=962).numpy()
+    ws = synthetic.scale_uniform(N, seed=963).numpy()
+    t = oracle.dequant_typed(acc, xs, ws, None, out_dtype=oracle.OUT_F32)
+    y = oracle.dequant_residual(acc, xs, ws, -t, None, out_dtype=oracle.OUT_F32)
+    assert np.all(y == 0.0)
+
+
+def test_residual_hand_example():
+    """acc = 12, xs = 0.5, ws = 0.25, bias = 1, r = 0.5: ((12 * 0.5) * 0.25 + 1) + 0.5 = 3."""
+    acc = np.array([[12]], np.int32)
+    y = oracle.dequant_residual(acc, np.array([0.5], np.float32), np.array([0.25], np.float32),
+                                np.array([[0.5]], np.float32), to_bf16_bits([1.0]), out_dtype=oracle.OUT_F32)
+    assert y[0, 0] == 3.0
+
+
+def test_residual_within_rounding_of_the_exact_value():
+    """Every fp32 step rounds once: the result is within 4 * 2^-24 * (|acc xs ws| +
+    |bias| + |r|) of the exact rational value (fp32 output)."""
+    M, N = 12, 20
+    g = np.random.default_rng(971)
+    acc = g.integers(-2 ** 22, 2 ** 22, size=(M, N)).astype(np.int32)
+    xs = synthetic.scale_uniform(M, seed=972).numpy()
+    ws = synthetic.scale_uniform(N, seed=973).numpy()
+    b = synthetic.normal_bf16((1, N), seed=974).reshape(N)
+    r = g.standard_normal((M, N)).astype(np.float32)
+    y = oracle.dequant_residual(acc, xs, ws, r, bits(b), out_dtype=oracle.OUT_F32)
+    bf = b.float().numpy()
+    for m in range(M):
+        for n in range(N):
+            prod = Fraction(int(acc[m, n])) * Fraction(float(xs[m])) * Fraction(float(ws[n]))
+            exact = prod + Fraction(float(bf[n])) + Fraction(float(r[m, n]))
+            bound = (abs(prod) + abs(Fraction(float(bf[n]))) + abs(Fraction(float(r[m, n])))) * Fraction(4, 2 ** 24)
+            assert abs(Fraction(float(y[m, n])) - exact) <= bound
