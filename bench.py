@@ -36,6 +36,8 @@ import torch  # noqa: E402
 from int8_weight_quantized_gb300 import synthetic  # noqa: E402
 
 METRIC = "INT8 linear TOPS (2MNK/s, fused dequant) and % of GB300 dense INT8 peak"
+# --path w8a16 times the layer's 16-bit-activation path instead (not the headline metric)
+METRICS = {"int8": METRIC, "w8a16": "W8A16 linear TOPS (2MNK/s, bf16 activations x int8 weight codes)"}
 UNIT = "TOPS"
 WORKLOADS = {spec[0]: spec for spec in synthetic.ALL_WORKLOADS}
 DEFAULT_WORKLOAD = synthetic.TENSORWISE_4096[0]
@@ -177,7 +179,7 @@ def workload_config(spec, l2_note):
 
 
 # ---------------------------------------------------------------- the CPU oracle arms
-def oracle_step_rows(case, rows):
+def oracle_step_rows(case, rows, path="int8"):
     """One oracle evaluation of the layer on the first `rows` rows (its own scale for
     tensorwise mode: the sample is the tensor)."""
     import numpy as np
@@ -190,7 +192,10 @@ def oracle_step_rows(case, rows):
         w, ws = case.w.numpy(), case.w_scale.numpy()
     b = None if case.bias is None else case.bias.contiguous().view(torch.int16).numpy().view(np.uint16)
     t0 = time.perf_counter()
-    oracle.int8_linear(x, w, ws, b, mode=case.mode)
+    if path == "w8a16":
+        oracle.w8a16_linear(x, w, ws, b, mode=case.mode)
+    else:
+        oracle.int8_linear(x, w, ws, b, mode=case.mode)
     return time.perf_counter() - t0
 
 
@@ -202,16 +207,16 @@ def prepare_oracle_case(spec):
     return case
 
 
-def cpu_baseline(spec, budget_s=12.0):
+def cpu_baseline(spec, path="int8", budget_s=12.0):
     """The oracle as it stands, on a bounded row sample of the workload."""
     import oracle
 
     case = prepare_oracle_case(spec)
     M, N, K = case.M, case.N, case.K
     probe = min(M, max(8, oracle.num_threads()))
-    t = oracle_step_rows(case, probe)
+    t = oracle_step_rows(case, probe, path)
     rows = int(min(M, max(probe, probe * budget_s / max(t, 1e-6))))
-    t = oracle_step_rows(case, rows)
+    t = oracle_step_rows(case, rows, path)
     return {"value": 2.0 * rows * N * K / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "first %d of %d rows x all %d columns, K=%d (%.1f s)" % (rows, M, N, K, t)}
 
@@ -226,18 +231,19 @@ def run_reference(args, spec):
     M, N, K = case.M, case.N, case.K
     budget = 150.0  # seconds for warmup + timed steps together
     probe = min(M, max(4, oracle.num_threads()))
-    t_probe = oracle_step_rows(case, probe)
+    t_probe = oracle_step_rows(case, probe, args.path)
     per_row = t_probe / probe
     rows = int(max(1, min(M, budget / (args.steps + args.warmup) / per_row)))
     for _ in range(args.warmup):
-        oracle_step_rows(case, rows)
-    times = [oracle_step_rows(case, rows) for _ in range(args.steps)]
+        oracle_step_rows(case, rows, args.path)
+    times = [oracle_step_rows(case, rows, args.path) for _ in range(args.steps)]
     step_s = sum(times) / len(times)
     value = 2.0 * rows * N * K / step_s / 1e12
     sample = "first %d of %d rows x all %d columns, K=%d, per step" % (rows, M, N, K)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+    line = {"impl": "reference", "metric": METRICS[args.path], "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8" if args.path == "int8" else "bf16",
+            "data": "synthetic",
             "config": workload_config(spec, "n/a (host)"),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": sample},
@@ -268,7 +274,11 @@ def run_ours(args, spec):
         ws_ = case.w_scale.to(dev)
     b = None if case.bias is None else case.bias.to(dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    work = ck.workspace(ck.ck_int8_linear_workspace_size(M, N, K, mode), dev)
+    w8a16 = args.path == "w8a16"
+    if w8a16:
+        work = ck.workspace(ck.load_library().ck_w8a16_linear_workspace_size(M, N, K, mode), dev)
+    else:
+        work = ck.workspace(ck.ck_int8_linear_workspace_size(M, N, K, mode), dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.zeros(CLEAN_BYTES // 8, dtype=torch.int64, device=dev)
     sink = torch.empty((), dtype=torch.int64, device=dev)
@@ -280,7 +290,10 @@ def run_ours(args, spec):
     ops = 2.0 * M * N * K
 
     def step():
-        ck.ck_int8_linear(x, w, ws_, b, mode=mode, y=y, ws=work)
+        if w8a16:
+            ck.ck_w8a16_linear(x, w, ws_, b, mode=mode, y=y, ws=work)
+        else:
+            ck.ck_int8_linear(x, w, ws_, b, mode=mode, y=y, ws=work)
 
     for i in range(args.warmup):
         flush_l2(i)
@@ -334,14 +347,19 @@ def run_ours(args, spec):
     p_n = prof["quantize"][1] + prof["widen"][1]
     gemm_avg_ms = reduce_max(g_ms / max(g_n, 1), dev)
     achieved = ops / (gemm_avg_ms * 1e-3) / 1e12
-    traffic = profiled_traffic(name)
+    traffic = None if w8a16 else profiled_traffic(name)
     # preparation, algorithmic bytes: read x (bf16) once, write its bf16 codes, read the
     # int8 weight, write its bf16 codes, plus the scales
-    prep_bytes = 2 * M * K + 2 * M * K + N * K + 2 * N * K + 4 * M
+    # (the 16-bit path: the weight widening, plus read x / write bf16(x @ H) for ConvRot)
+    if w8a16:
+        prep_bytes = N * K + 2 * N * K + (4 * M * K if mode == synthetic.CONVROT else 0)
+    else:
+        prep_bytes = 2 * M * K + 2 * M * K + N * K + 2 * N * K + 4 * M
     p_step = max(p_ms, 1e-9) / kt_steps
     roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
                 "frac": achieved / bf16_peak, "traffic": traffic,
-                "kernel": "gemm_kernel (tcgen05 kind::f16 on int8 codes, exact int32, fused dequant)",
+                "kernel": ("gemm_kernel<mixed> (tcgen05 kind::f16, bf16 activations x int8 codes, fp32 sum)" if w8a16
+                           else "gemm_kernel (tcgen05 kind::f16 on int8 codes, exact int32, fused dequant)"),
                 "peak_source": "%s bf16 dense (burst); sustained %.1f" % (provenance, bf16_sust),
                 "avg_launch_ms": gemm_avg_ms, "timed_launches": g_n}
     kernels = {
@@ -370,14 +388,14 @@ def run_ours(args, spec):
     e2e = {"value": world * ops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,
            "d2h_bytes_per_step": y_host.numel() * 2, "ms_per_step": e2e_ms}
 
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+    line = {"metric": METRICS[args.path], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "vs_baseline": None, "dtype": "int8" if not w8a16 else "bf16", "data": "synthetic",
             "config": workload_config(spec, "flushed between steps (%d MiB write, then %d MiB read)" % (FLUSH_BYTES >> 20, CLEAN_BYTES >> 20)),
             "roofline": roofline, "kernels": kernels, "e2e": e2e, "clocks": clocks,
             "gpu_launches": int(sum(n for _, n in counts.values())), "timed_wall_s": wall}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(spec)
+        line["cpu_baseline"] = cpu_baseline(spec, args.path)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if torch.distributed.is_initialized():
@@ -393,6 +411,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=sorted(METRICS), default="int8",
+                    help="int8: the INT8 layer (the headline); w8a16: its 16-bit-activation path")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -120,15 +120,18 @@ size_t ck_int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
  *            the pre-rotated, per-row quantized W @ H^T, used as is.
  *   w_scale: fp32 [N] (CK_PER_ROW, CK_CONVROT) or fp32 [1] (CK_TENSORWISE).
  *   bias:    bf16 [N] or NULL.
+ *   residual: [M,N] of out_dtype or NULL, added after the bias (issue #280, "Kernel
+ *            used", mentions residual-fused calls); may be y itself (in-place update).
  *   y:       [M,N] of out_dtype (a ck_dtype_t), written.
- *            y = out(((float(acc) * xs) * ws) + bias) with every fp32 operation rounded
- *            separately, in that order, and out the rounding of ck_dtype_t.
+ *            y = out((((float(acc) * xs) * ws) + bias) + residual) with every fp32
+ *            operation rounded separately, in that order, and out the rounding of
+ *            ck_dtype_t.
  *   workspace/workspace_bytes: device scratch of ck_int8_linear_workspace_size() bytes.
  * No int32 intermediate is ever written to device memory.  An out_dtype outside
  * ck_dtype_t gives CK_ERR_INVALID_ARG. */
-int ck_int8_linear(const void *x, const int8_t *w, const float *w_scale, const void *bias, void *y, int64_t M,
-                   int64_t N, int64_t K, int mode, int out_dtype, void *workspace, size_t workspace_bytes,
-                   void *stream);
+int ck_int8_linear(const void *x, const int8_t *w, const float *w_scale, const void *bias, const void *residual,
+                   void *y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype, void *workspace,
+                   size_t workspace_bytes, void *stream);
 
 /* ConvRot weight preparation (issue #278, "Suggested fix": the stored weight is
  * W_rot = W @ H^T; since H is symmetric, row n of it is row n of W times H), quantized
@@ -145,28 +148,29 @@ int ck_convrot_prepare_weight(const float *W, int64_t N, int64_t K, int8_t *w, f
  * weight dequantized on the fly, the GEMM on 16-bit tensor cores, the weight keeping its
  * INT8 footprint; for ConvRot the activation rotated online and the weight used as
  * stored, in the rotated basis).  No activation quantize:
- *   y[m,n] = out( fp32( sum_k a[m,k] * w[n,k] ) * w_scale[n] + bias[n] )
+ *   y[m,n] = out( (fp32( sum_k a[m,k] * w[n,k] ) * w_scale[n] + bias[n]) + residual[m,n] )
  *   a = x (CK_TENSORWISE, CK_PER_ROW) or bf16_rne(x @ H) (CK_CONVROT, K % 128 == 0; the
  *   fp32 block transform of ck_quantize_int8_rowwise, rounded once).
  * The codes are exact in bf16; the sum over all of K is accumulated in fp32 by the tensor
  * cores (rounding order not specified: error at most about K * 2^-24 * sum_k |a w|),
  * then scaled, biased and rounded to out_dtype like ck_int8_linear's epilogue.
- *   x, w, w_scale (fp32 [1] for CK_TENSORWISE, else [N]), bias, y, out_dtype: as for
- *   ck_int8_linear.  workspace: ck_w8a16_linear_workspace_size() bytes (the widened
+ *   x, w, w_scale (fp32 [1] for CK_TENSORWISE, else [N]), bias, residual, y, out_dtype:
+ *   as for ck_int8_linear.  workspace: ck_w8a16_linear_workspace_size() bytes (the widened
  *   weight, and the rotated activation for ConvRot). */
 size_t ck_w8a16_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
-int ck_w8a16_linear(const void *x, const int8_t *w, const float *w_scale, const void *bias, void *y, int64_t M,
-                    int64_t N, int64_t K, int mode, int out_dtype, void *workspace, size_t workspace_bytes,
-                    void *stream);
+int ck_w8a16_linear(const void *x, const int8_t *w, const float *w_scale, const void *bias, const void *residual,
+                    void *y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype, void *workspace,
+                    size_t workspace_bytes, void *stream);
 
 /* GEMM + fused dequant on an already-quantized activation (the second half of
  * ck_int8_linear): q int8 [M,K], x_scale fp32 [M] (or [1] if scalar_scales), w int8
- * [N,K], w_scale fp32 [N] (or [1]), bias bf16 [N] or NULL, y [M,N] of out_dtype
- * (a ck_dtype_t).  workspace: ck_int8_gemm_workspace_size(M, N, K) bytes. */
+ * [N,K], w_scale fp32 [N] (or [1]), bias bf16 [N] or NULL, residual [M,N] of out_dtype
+ * or NULL (may be y), y [M,N] of out_dtype (a ck_dtype_t).
+ * workspace: ck_int8_gemm_workspace_size(M, N, K) bytes. */
 size_t ck_int8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 int ck_int8_gemm_dequant(const int8_t *q, const float *x_scale, const int8_t *w, const float *w_scale,
-                         const void *bias, void *y, int64_t M, int64_t N, int64_t K, int scalar_scales,
-                         int out_dtype, void *workspace, size_t workspace_bytes, void *stream);
+                         const void *bias, const void *residual, void *y, int64_t M, int64_t N, int64_t K,
+                         int scalar_scales, int out_dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /* The raw int32 accumulators acc[m,n] = sum_k q[m,k] w[n,k] of the same GEMM engine,
  * written to acc int32 [M,N] (for exactness checks; the fused path never writes them).

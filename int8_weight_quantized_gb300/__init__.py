@@ -49,12 +49,12 @@ def load_library(path=None):
         "ck_quantize_int8_tensorwise": ([P, I64, I64, P, P, P, SZ, P], I),
         "ck_quantize_int8_tensorwise_noalloc": ([P, I64, I64, P, P, P], I),
         "ck_int8_linear_workspace_size": ([I64, I64, I64, I], SZ),
-        "ck_int8_linear": ([P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
+        "ck_int8_linear": ([P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_convrot_prepare_weight": ([P, I64, I64, P, P, P], I),
         "ck_int8_gemm_workspace_size": ([I64, I64, I64], SZ),
         "ck_w8a16_linear_workspace_size": ([I64, I64, I64, I], SZ),
-        "ck_w8a16_linear": ([P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
-        "ck_int8_gemm_dequant": ([P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
+        "ck_w8a16_linear": ([P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
+        "ck_int8_gemm_dequant": ([P, P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_int8_gemm_s32": ([P, P, P, I64, I64, I64, P, SZ, P], I),
         "ck_profile_begin": ([I], I),
         "ck_profile_end": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I], I),
@@ -162,8 +162,16 @@ def _out_code(out_dtype):
     return OUT_DTYPES[out_dtype]
 
 
-def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stream=None, out_dtype=torch.bfloat16):
-    """y [M,N] of out_dtype = dequant(int32 GEMM(quantize(x [@ H]), w)) (+ bias)."""
+def _residual(residual, out_dtype, M, N):
+    if residual is not None:
+        _req(residual, out_dtype, (M, N), "residual")
+    return residual
+
+
+def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stream=None, out_dtype=torch.bfloat16,
+                   residual=None):
+    """y [M,N] of out_dtype = dequant(int32 GEMM(quantize(x [@ H]), w)) (+ bias) (+ residual);
+    residual has y's type and shape and may be y itself."""
     code = _out_code(out_dtype)
     M, K = x.shape
     N = w.shape[0]
@@ -177,13 +185,15 @@ def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stre
     L = load_library()
     need = L.ck_int8_linear_workspace_size(M, N, K, int(mode))
     ws = workspace(need, x.device) if ws is None else ws
-    _check(L.ck_int8_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, int(mode), code,
-                            _ptr(ws), ws.numel(), _stream(stream)))
+    _residual(residual, out_dtype, M, N)
+    _check(L.ck_int8_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(residual), _ptr(y), M, N, K, int(mode),
+                            code, _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 
-def ck_w8a16_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stream=None, out_dtype=torch.bfloat16):
-    """y [M,N] of out_dtype = (bf16 x [@ H]) . (int8 w)^T summed in fp32, * w_scale (+ bias)."""
+def ck_w8a16_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stream=None, out_dtype=torch.bfloat16,
+                    residual=None):
+    """y [M,N] of out_dtype = (bf16 x [@ H]) . (int8 w)^T summed in fp32, * w_scale (+ bias) (+ residual)."""
     code = _out_code(out_dtype)
     M, K = x.shape
     N = w.shape[0]
@@ -197,8 +207,9 @@ def ck_w8a16_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, str
     L = load_library()
     need = L.ck_w8a16_linear_workspace_size(M, N, K, int(mode))
     ws = workspace(need, x.device) if ws is None else ws
-    _check(L.ck_w8a16_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, int(mode), code,
-                             _ptr(ws), ws.numel(), _stream(stream)))
+    _residual(residual, out_dtype, M, N)
+    _check(L.ck_w8a16_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(residual), _ptr(y), M, N, K,
+                             int(mode), code, _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 
@@ -215,7 +226,7 @@ def ck_convrot_prepare_weight(W, w=None, w_scale=None, stream=None):
 
 
 def ck_int8_gemm_dequant(q, x_scale, w, w_scale, bias=None, scalar_scales=False, y=None, ws=None, stream=None,
-                         out_dtype=torch.bfloat16):
+                         out_dtype=torch.bfloat16, residual=None):
     """GEMM + fused dequant on pre-quantized q int8 [M,K]; returns y [M,N] of out_dtype."""
     code = _out_code(out_dtype)
     M, K = q.shape
@@ -231,8 +242,9 @@ def ck_int8_gemm_dequant(q, x_scale, w, w_scale, bias=None, scalar_scales=False,
     L = load_library()
     need = L.ck_int8_gemm_workspace_size(M, N, K)
     ws = workspace(need, q.device) if ws is None else ws
-    _check(L.ck_int8_gemm_dequant(_ptr(q), _ptr(x_scale), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K,
-                                  int(bool(scalar_scales)), code, _ptr(ws), ws.numel(), _stream(stream)))
+    _residual(residual, out_dtype, M, N)
+    _check(L.ck_int8_gemm_dequant(_ptr(q), _ptr(x_scale), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(residual), _ptr(y),
+                                  M, N, K, int(bool(scalar_scales)), code, _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 

@@ -312,9 +312,9 @@ static bool valid_out_dtype(int t)
     return t == CK_OUT_BF16 || t == CK_OUT_F16 || t == CK_OUT_F32;
 }
 
-int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const void* bias, void* y, int64_t M,
-                   int64_t N, int64_t K, int mode, int out_dtype, void* workspace, size_t workspace_bytes,
-                   void* stream)
+int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const void* bias, const void* residual,
+                   void* y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype, void* workspace,
+                   size_t workspace_bytes, void* stream)
 {
     if (mode != CK_TENSORWISE && mode != CK_PER_ROW && mode != CK_CONVROT)
         return fail(CK_ERR_INVALID_ARG, "mode must be 0 (tensorwise), 1 (per-row) or 2 (ConvRot), got %d", mode);
@@ -334,6 +334,8 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
     CK_REQUIRE_PTR(workspace);
     if (bias != nullptr && !aligned16(bias))
         return fail(CK_ERR_INVALID_ARG, "bias must be 16-byte aligned");
+    if (residual != nullptr && !aligned16(residual))
+        return fail(CK_ERR_INVALID_ARG, "residual must be 16-byte aligned");
     const size_t need = ck_int8_linear_workspace_size(M, N, K, mode);
     if (workspace_bytes < need)
         return fail(CK_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
@@ -368,6 +370,7 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
     p.bias = bias;
     p.scalar_scales = mode == CK_TENSORWISE;
     p.y = y;
+    p.residual = residual;
     p.out_dtype = out_dtype;
     p.tail = ws.tail;
     std::string why;
@@ -393,9 +396,9 @@ size_t ck_w8a16_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode)
     return w8a16_ws_bytes(M, N, K, mode);
 }
 
-int ck_w8a16_linear(const void* x, const int8_t* w, const float* w_scale, const void* bias, void* y, int64_t M,
-                    int64_t N, int64_t K, int mode, int out_dtype, void* workspace, size_t workspace_bytes,
-                    void* stream)
+int ck_w8a16_linear(const void* x, const int8_t* w, const float* w_scale, const void* bias, const void* residual,
+                    void* y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype, void* workspace,
+                    size_t workspace_bytes, void* stream)
 {
     if (mode != CK_TENSORWISE && mode != CK_PER_ROW && mode != CK_CONVROT)
         return fail(CK_ERR_INVALID_ARG, "mode must be 0 (tensorwise), 1 (per-row) or 2 (ConvRot), got %d", mode);
@@ -415,6 +418,8 @@ int ck_w8a16_linear(const void* x, const int8_t* w, const float* w_scale, const 
     CK_REQUIRE_PTR(workspace);
     if (bias != nullptr && !aligned16(bias))
         return fail(CK_ERR_INVALID_ARG, "bias must be 16-byte aligned");
+    if (residual != nullptr && !aligned16(residual))
+        return fail(CK_ERR_INVALID_ARG, "residual must be 16-byte aligned");
     const size_t need = w8a16_ws_bytes(M, N, K, mode);
     if (workspace_bytes < need)
         return fail(CK_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
@@ -447,6 +452,7 @@ int ck_w8a16_linear(const void* x, const int8_t* w, const float* w_scale, const 
     p.bias = bias;
     p.scalar_scales = mode == CK_TENSORWISE;
     p.y = y;
+    p.residual = residual;
     p.out_dtype = out_dtype;
     p.mixed = true;
     std::string why;
@@ -489,8 +495,9 @@ size_t ck_int8_gemm_workspace_size(int64_t M, int64_t N, int64_t K)
 }
 
 static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, const float* w_scale, const void* bias,
-                      void* y, int32_t* acc, int64_t M, int64_t N, int64_t K, int scalar_scales, int out_dtype,
-                      void* workspace, size_t workspace_bytes, void* stream, const char* name)
+                      const void* residual, void* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                      int scalar_scales, int out_dtype, void* workspace, size_t workspace_bytes, void* stream,
+                      const char* name)
 {
     if (acc == nullptr && !valid_out_dtype(out_dtype))
         return fail(CK_ERR_INVALID_ARG, "out_dtype must be 0 (bf16), 1 (fp16) or 2 (fp32), got %d", out_dtype);
@@ -508,6 +515,8 @@ static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, co
         CK_REQUIRE_PTR(y);
         if (bias != nullptr && !aligned16(bias))
             return fail(CK_ERR_INVALID_ARG, "bias must be 16-byte aligned");
+        if (residual != nullptr && !aligned16(residual))
+            return fail(CK_ERR_INVALID_ARG, "residual must be 16-byte aligned");
     } else {
         CK_REQUIRE_PTR(acc);
     }
@@ -543,6 +552,7 @@ static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, co
     p.bias = bias;
     p.scalar_scales = scalar_scales != 0;
     p.y = acc ? nullptr : y;
+    p.residual = acc ? nullptr : residual;
     p.out_dtype = out_dtype;
     p.acc = acc;
     p.tail = tail;
@@ -557,17 +567,17 @@ static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, co
 }
 
 int ck_int8_gemm_dequant(const int8_t* q, const float* x_scale, const int8_t* w, const float* w_scale,
-                         const void* bias, void* y, int64_t M, int64_t N, int64_t K, int scalar_scales,
-                         int out_dtype, void* workspace, size_t workspace_bytes, void* stream)
+                         const void* bias, const void* residual, void* y, int64_t M, int64_t N, int64_t K,
+                         int scalar_scales, int out_dtype, void* workspace, size_t workspace_bytes, void* stream)
 {
-    return gemm_entry(q, x_scale, w, w_scale, bias, y, nullptr, M, N, K, scalar_scales, out_dtype, workspace,
-                      workspace_bytes, stream, "int8_gemm_dequant");
+    return gemm_entry(q, x_scale, w, w_scale, bias, residual, y, nullptr, M, N, K, scalar_scales, out_dtype,
+                      workspace, workspace_bytes, stream, "int8_gemm_dequant");
 }
 
 int ck_int8_gemm_s32(const int8_t* q, const int8_t* w, int32_t* acc, int64_t M, int64_t N, int64_t K,
                      void* workspace, size_t workspace_bytes, void* stream)
 {
-    return gemm_entry(q, nullptr, w, nullptr, nullptr, nullptr, acc, M, N, K, 0, CK_OUT_BF16, workspace,
+    return gemm_entry(q, nullptr, w, nullptr, nullptr, nullptr, nullptr, acc, M, N, K, 0, CK_OUT_BF16, workspace,
                       workspace_bytes, stream, "int8_gemm_s32");
 }
 

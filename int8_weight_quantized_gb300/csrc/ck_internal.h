@@ -42,6 +42,7 @@ struct GemmProblem {
     const float* x_scale = nullptr;
     const float* w_scale = nullptr;
     const void* bias = nullptr;  // bf16 [N] or nullptr
+    const void* residual = nullptr;  // [M,N] of the output type or nullptr (may alias y)
     int scalar_scales = 0;
     void* y = nullptr;           // [M,N] of the output type
     int out_dtype = 0;           // 0 bf16, 1 fp16, 2 fp32

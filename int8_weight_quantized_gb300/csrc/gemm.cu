@@ -103,6 +103,7 @@ struct Args {
     const float* xs;
     const float* ws;
     const __nv_bfloat16* bias;
+    const void* residual;   // [M,N] of the output type, added after the bias; may alias y
     int32_t* acc;
     int64_t num_units;      // pair-tiles (pairs) or tiles
     int unit_rows;          // tile rows per unit: 2 (pairs) or 1
@@ -213,6 +214,31 @@ struct OutType {
     static constexpr int BOX_COLS = (int)OUT_ROW_BYTES / BYTES;  // 32 (16-bit types) or 16 (fp32)
     static constexpr int PER_CHUNK = 16 / BYTES;                   // values per 16-byte chunk
 };
+
+// 16 bytes of output-type values -> fp32 (exact).
+template <int OUT>
+__device__ __forceinline__ void unpack_out(const uint4& r, float (&v)[OutType<OUT>::PER_CHUNK])
+{
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    if (OUT == kOutF32) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v[i] = __uint_as_float(w[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (OUT == kOutF16) {
+                const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+                v[2 * i] = __low2float(h);
+                v[2 * i + 1] = __high2float(h);
+            } else {
+                const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+                v[2 * i] = __low2float(h);
+                v[2 * i + 1] = __high2float(h);
+            }
+        }
+    }
+}
 
 // Round two fp32 values to the output type and pack them (lower column first).
 template <int OUT>
@@ -592,6 +618,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                             for (int i = 0; i < PC; ++i)
                                 wsv[i] = bv[i] = 0.0f;
                         }
+                        // this lane's residual: 16 bytes of its own row (the element it writes)
+                        float rv[PC];
+                        if (args.residual != nullptr && row < args.M && col < args.N) {
+                            const uint4 rr = __ldcg(reinterpret_cast<const uint4*>(
+                                static_cast<const uint8_t*>(args.residual) + (row * args.N + col) * OT::BYTES));
+                            unpack_out<OUT>(rr, rv);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < PC; ++i)
+                                rv[i] = 0.0f;
+                        }
                         float t[PC];
 #pragma unroll
                         for (int i = 0; i < PC; ++i) {
@@ -604,6 +641,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             t[i] = __fmul_rn(t[i], wsv[i]);
                             if (args.bias)
                                 t[i] = __fadd_rn(t[i], bv[i]);
+                            if (args.residual)
+                                t[i] = __fadd_rn(t[i], rv[i]);
                         }
                         uint32_t packed[4];
                         if (OUT == kOutF32) {
@@ -995,6 +1034,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.xs = p.x_scale;
     a.ws = p.w_scale;
     a.bias = reinterpret_cast<const __nv_bfloat16*>(p.bias);
+    a.residual = p.residual;
     a.acc = p.acc;
     a.tiles_m = (int)((p.M + BM - 1) / BM);
     a.num_kb = (int)((p.K + BK - 1) / BK);

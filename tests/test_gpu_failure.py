@@ -39,11 +39,11 @@ def test_bad_arguments_on_real_buffers():
     P = ctypes.c_void_p
     stream = P(torch.cuda.current_stream().cuda_stream)
     # misaligned activation pointer
-    st = L.ck_int8_linear(P(x.data_ptr() + 2), P(w.data_ptr()), P(ws.data_ptr()), None, P(y.data_ptr()), 16, 16, 64,
+    st = L.ck_int8_linear(P(x.data_ptr() + 2), P(w.data_ptr()), P(ws.data_ptr()), None, None, P(y.data_ptr()), 16, 16, 64,
                           1, 0, P(work.data_ptr()), work.numel(), stream)
     assert st == ck.CK_ERR_INVALID_ARG and "aligned" in ck.ck_last_error()
     # workspace too small
-    st = L.ck_int8_linear(P(x.data_ptr()), P(w.data_ptr()), P(ws.data_ptr()), None, P(y.data_ptr()), 16, 16, 64,
+    st = L.ck_int8_linear(P(x.data_ptr()), P(w.data_ptr()), P(ws.data_ptr()), None, None, P(y.data_ptr()), 16, 16, 64,
                           1, 0, P(work.data_ptr()), 64, stream)
     assert st == ck.CK_ERR_INVALID_ARG and "workspace" in ck.ck_last_error()
     torch.cuda.synchronize()

@@ -254,3 +254,45 @@ def test_split_tail_dequant(monkeypatch, out_dtype):
     y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), out_dtype=out_dtype)
     torch.cuda.synchronize()
     assert ulp_distance(out_bits(y), ref).max() <= MAX_ULP
+
+
+def residual_case(M, N, out_dtype, seed):
+    r = synthetic.normal_bf16((M, N), seed=seed, std=2.0).to(out_dtype)
+    return r, r.float().numpy()
+
+
+@pytest.mark.parametrize("out_dtype,code", TYPED)
+@pytest.mark.parametrize("inplace", [False, True])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (129, 264, 1040), (1, 8, 16)])
+def test_dequant_residual(M, N, K, inplace, out_dtype, code):
+    """y = out(((acc * xs) * ws + bias) + residual), the residual in y's type; in place
+    (residual is y) as well."""
+    q = synthetic.int8_uniform((M, K), seed=81 + M)
+    w = synthetic.int8_uniform((N, K), seed=82 + N)
+    xs = synthetic.scale_uniform(M, seed=83, mul=0.02)
+    ws = synthetic.scale_uniform(N, seed=84, mul=0.01)
+    b = synthetic.normal_bf16((1, N), seed=85, std=0.5).reshape(N)
+    r, r_np = residual_case(M, N, out_dtype, seed=86)
+    acc = oracle.gemm_s32(q.numpy(), w.numpy())
+    ref = oracle.dequant_residual(acc, xs.numpy(), ws.numpy(), r_np, bits(b), out_dtype=code)
+    ref = ref.view(np.uint32) if code == oracle.OUT_F32 else ref
+    r_dev = r.to(DEV)
+    y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), out_dtype=out_dtype,
+                                residual=r_dev, y=r_dev if inplace else None)
+    torch.cuda.synchronize()
+    d = ulp_distance(out_bits(y), ref)
+    assert d.max() <= MAX_ULP, "max ulp %d" % d.max()
+
+
+def test_residual_after_a_split_tail(monkeypatch):
+    monkeypatch.setenv("CK_GEMM_SPLIT", "3")
+    M, N, K = 512, 1024, 2048
+    q = synthetic.int8_uniform((M, K), seed=91)
+    w = synthetic.int8_uniform((N, K), seed=92)
+    xs = synthetic.scale_uniform(M, seed=93, mul=0.02)
+    ws = synthetic.scale_uniform(N, seed=94, mul=0.01)
+    r, r_np = residual_case(M, N, torch.bfloat16, seed=95)
+    ref = oracle.dequant_residual(oracle.gemm_s32(q.numpy(), w.numpy()), xs.numpy(), ws.numpy(), r_np, None)
+    y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), None, residual=r.to(DEV))
+    torch.cuda.synchronize()
+    assert bf16_ulp_distance(bits(y), ref).max() <= MAX_ULP

@@ -111,3 +111,26 @@ def test_sweep_large_shapes_sampled(spec):
 def test_large_index_boundary_sampled(spec):
     assert spec[1] * spec[2] >= 2 ** 31 - 21504  # straddles the int32 element-offset limit
     run_sampled(spec)
+
+
+@pytest.mark.parametrize("mode", [synthetic.TENSORWISE, synthetic.PER_ROW, synthetic.CONVROT])
+def test_linear_residual_in_place(mode):
+    """A residual-stream update y += layer(x), in place, through the whole layer."""
+    M, N, K = 300, 264, 1152
+    x = synthetic.normal_bf16((M, K), seed=71 + mode)
+    if mode == synthetic.CONVROT:
+        w, ws = oracle.prepare_convrot_weight(synthetic.normal_f32((N, K), seed=72, std=0.02).numpy())
+        w, ws = torch.from_numpy(w), torch.from_numpy(ws)
+    else:
+        w = synthetic.int8_uniform((N, K), seed=72)
+        ws = synthetic.scale_uniform(1 if mode == synthetic.TENSORWISE else N, seed=73)
+    b = synthetic.normal_bf16((1, N), seed=74, std=0.5).reshape(N)
+    r = synthetic.normal_bf16((M, N), seed=75, std=3.0)
+    ref8 = oracle.int8_linear(bits(x), w.numpy(), ws.numpy(), bits(b), mode=mode)
+    ref = oracle.dequant_residual(ref8["acc"], ref8["xs"], ws.numpy(), r.float().numpy(), bits(b),
+                                  scalar_scales=(mode == synthetic.TENSORWISE))
+    y = r.to(DEV)
+    ck.ck_int8_linear(x.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), mode=mode, y=y, residual=y)
+    torch.cuda.synchronize()
+    d = bf16_ulp_distance(bits(y), ref)
+    assert d.max() <= MAX_ULP, "max ulp %d" % d.max()

@@ -119,3 +119,20 @@ def test_w8a16_rejects_bad_arguments():
     with pytest.raises(ck.CkError) as e:
         ck.ck_w8a16_linear(x, w, torch.ones(8, device=DEV), mode=ck.CONVROT)  # K % 128
     assert "128" in str(e.value)
+
+
+@pytest.mark.parametrize("mode", [synthetic.PER_ROW, synthetic.CONVROT])
+def test_w8a16_residual(mode):
+    """The residual is one more fp32 add: the bound gains 2^-24 * |residual|."""
+    M, N, K = 129, 264, 1152
+    x, w, ws, b = make(M, N, K, mode, seed=11)
+    r = synthetic.normal_bf16((M, N), seed=12, std=2.0)
+    y_ref, mag = oracle.w8a16_linear(bits(x), w.numpy(), ws.numpy(), bits(b), mode=mode)
+    rf = r.float().numpy().astype(np.float64)
+    y = ck.ck_w8a16_linear(x.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), mode=mode, residual=r.to(DEV))
+    torch.cuda.synchronize()
+    got = y.float().cpu().numpy().astype(np.float64)
+    ref = y_ref + rf
+    babs = np.abs(b.float().numpy().astype(np.float64))[None, :]
+    tol = ulp(ref, 8) + 2.0 ** -24 * (K + 8) * (mag + babs + np.abs(rf))
+    assert np.all(np.abs(got - ref) <= tol)

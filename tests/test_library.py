@@ -54,8 +54,8 @@ def _call_linear(lib, M, N, K, mode, **kw):
     ptr = P(4096)  # never dereferenced: validation fails first
     args = dict(x=ptr, w=ptr, ws=ptr, bias=None, y=ptr, work=ptr, nbytes=1 << 40, out_dtype=0)
     args.update(kw)
-    return lib.ck_int8_linear(args["x"], args["w"], args["ws"], args["bias"], args["y"], M, N, K, mode,
-                              args["out_dtype"], args["work"], args["nbytes"], None)
+    return lib.ck_int8_linear(args["x"], args["w"], args["ws"], args["bias"], args.get("residual"), args["y"], M, N, K,
+                              mode, args["out_dtype"], args["work"], args["nbytes"], None)
 
 
 @pytest.mark.parametrize("M,N,K,mode,what", [
@@ -80,7 +80,7 @@ def test_unknown_output_type_is_rejected(lib):
     assert "out_dtype" in ck.ck_last_error()
     import ctypes
     P = ctypes.c_void_p(4096)
-    st = lib.ck_int8_gemm_dequant(P, P, P, P, None, P, 16, 16, 32, 0, -1, P, 1 << 40, None)
+    st = lib.ck_int8_gemm_dequant(P, P, P, P, None, None, P, 16, 16, 32, 0, -1, P, 1 << 40, None)
     assert st == ck.CK_ERR_INVALID_ARG and "out_dtype" in ck.ck_last_error()
     with pytest.raises(ValueError):
         ck.ck_int8_linear(torch.zeros((16, 32), dtype=torch.bfloat16), torch.zeros((16, 32), dtype=torch.int8),
@@ -96,6 +96,8 @@ def test_null_and_misaligned_pointers_are_rejected(lib):
     assert "16-byte aligned" in ck.ck_last_error()
     assert _call_linear(lib, 16, 16, 32, 1, nbytes=10) == ck.CK_ERR_INVALID_ARG
     assert "workspace too small" in ck.ck_last_error()
+    assert _call_linear(lib, 16, 16, 32, 1, residual=ctypes.c_void_p(4104)) == ck.CK_ERR_INVALID_ARG
+    assert "residual must be 16-byte aligned" in ck.ck_last_error()
 
 
 def test_no_device_is_reported_not_faked(lib):
