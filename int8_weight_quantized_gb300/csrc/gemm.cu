@@ -134,10 +134,11 @@ struct Item {
     int slice;      // -1: the whole K range
 };
 
+template <bool SPLIT>
 __device__ __forceinline__ Item item_of(int64_t it, const Args& a)
 {
     Item r;
-    if (it < a.full_units) {
+    if (!SPLIT || it < a.full_units) {
         r.unit = it;
         r.tail = 0;
         r.kb_begin = 0;
@@ -259,7 +260,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 // sub-partition as well).
 // MIXED: 16-bit activations times int8 weight codes (both bf16 operands), the fp32
 // accumulation over all of K kept in TMEM, epilogue (sum * w_scale) + bias.
-template <bool RAW, bool PAIR, int OUT, bool MIXED>
+// SPLIT: the launch splits its last partial wave along K (the code for it lives only in
+// these instances, so the common kernel keeps its own, smaller code).
+template <bool RAW, bool PAIR, int OUT, bool MIXED, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const Args args)
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t issued_parity = 0;     // parity of that load's phase, per stage
                 bool ok = true;
                 for (int64_t it = cluster; ok && it < args.num_items; it += clusters) {
-                    const Item w = item_of(it, args);
+                    const Item w = item_of<SPLIT>(it, args);
                     int um, nb;
                     unit_coords(w.unit, args, um, nb);
                     const int32_t m0 = (um * args.unit_rows + rank) * BM, n0 = nb * args.bn;
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t acc_iter = 0;
                 bool ok = true;
                 for (int64_t it = cluster; ok && it < args.num_items; it += clusters) {
-                    const Item w = item_of(it, args);
+                    const Item w = item_of<SPLIT>(it, args);
                     for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += args.chunk_kb) {
                         const uint32_t buf = acc_iter & 1u;
                         const uint32_t acc_phase = (acc_iter >> 1) & 1u;
@@ -455,7 +458,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t nstore = 0;
         bool ok = true;
         for (int64_t it = cluster; ok && it < args.num_items; it += clusters) {
-            const Item w = item_of(it, args);
+            const Item w = item_of<SPLIT>(it, args);
             int um, nb;
             unit_coords(w.unit, args, um, nb);
             const int64_t m0 = (int64_t)(um * args.unit_rows + rank) * BM;
@@ -517,7 +520,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok)
                 break;
 
-            if (w.slice >= 0 && ncols > 0) {
+            if (SPLIT && w.slice >= 0 && ncols > 0) {
                 // one K-slice of a tail unit: publish this warp's sums; the last slice to
                 // arrive adds the others' and goes on to the epilogue
                 constexpr int RANKS = PAIR ? 2 : 1;
@@ -573,9 +576,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
                 using OT = OutType<OUT>;
                 constexpr int PC = OT::PER_CHUNK;
+                constexpr int BOX = OT::BOX_COLS;
                 const int64_t row0 = m0 + quarter * 32;
-#pragma unroll
-                for (int g = 0; g < 128 / OT::BOX_COLS; ++g) {
+                // A rolled loop over the boxes: its body is fetched once per tile.  The store
+                // loop first runs with cold instruction caches (the bench's L2 flush evicts
+                // code too); unrolled, that first pass held up the epilogue long enough for
+                // both accumulators to fill and the MMAs to stall.  Each box converts
+                // run[0 .. BOX) and shifts the sums down by BOX, so indices stay compile-time.
+#pragma unroll 1
+                for (int g = 0; g < 128 / BOX; ++g) {
                     const int64_t col0 = cbase + g * OT::BOX_COLS;
                     if (g * OT::BOX_COLS >= ncols || col0 >= args.N || row0 >= args.M)
                         break;  // warp-uniform: nothing of this box is inside the tile and y
@@ -585,7 +594,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     __syncwarp();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {  // one 16-byte chunk of the row: PC columns
-                        const int j0 = g * OT::BOX_COLS + c * PC;  // first running sum of the chunk
+                        const int j0 = c * PC;  // first running sum of the chunk (after the shifts)
                         const int64_t col = col0 + c * PC;
                         // the same columns for every lane: broadcast loads, L1 hits after the
                         // first tile of a column range
@@ -666,6 +675,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         bulk_commit_group();
                     }
                     ++nstore;
+#pragma unroll
+                    for (int j = 0; j < 128 - BOX; ++j)
+                        run[j] = run[j + BOX];
                 }
             }
         }
@@ -753,7 +765,7 @@ static bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ba
     return true;
 }
 
-template <bool RAW, bool PAIR, int OUT, bool MIXED>
+template <bool RAW, bool PAIR, int OUT, bool MIXED, bool SPLIT>
 static cudaError_t ensure_smem_attr(int device)
 {
     static bool done[64] = {};
@@ -761,7 +773,7 @@ static cudaError_t ensure_smem_attr(int device)
     std::lock_guard<std::mutex> lock(mu);
     if (device >= 0 && device < 64 && done[device])
         return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR, OUT, MIXED>,
+    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)gemm::Mode<PAIR>::SMEM_BYTES);
     if (e == cudaSuccess) {
@@ -769,7 +781,7 @@ static cudaError_t ensure_smem_attr(int device)
         // with (registers are granted per warp in units of 8 per thread), else the
         // epilogue's increase would wait forever: refuse to launch instead
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<RAW, PAIR, OUT, MIXED>);
+        e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT>);
         if (e == cudaSuccess &&
             (uint64_t)((fa.numRegs + 7) / 8 * 8) * gemm::THREADS < (uint64_t)gemm::REGS_NEEDED_PER_BLOCK)
             e = cudaErrorInvalidConfiguration;
@@ -810,13 +822,13 @@ static cudaError_t resident_units(const DeviceInfo& dev, int64_t* out)
     std::lock_guard<std::mutex> lock(mu);
     int& n = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
     if (n == 0) {
-        cudaError_t e = ensure_smem_attr<false, true, gemm::kOutBf16, false>(dev.device);
+        cudaError_t e = ensure_smem_attr<false, true, gemm::kOutBf16, false, false>(dev.device);
         if (e != cudaSuccess)
             return e;
         cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = make_config(true, gemm::Mode<true>::SMEM_BYTES, nullptr, attr);
         cfg.gridDim = dim3(2 * (dev.sm_count / 2));
-        e = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_kernel<false, true, gemm::kOutBf16, false>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_kernel<false, true, gemm::kOutBf16, false, false>, &cfg);
         if (e != cudaSuccess)
             return e;
         if (n <= 0)
@@ -927,12 +939,12 @@ static void choose_tile(int64_t M, int64_t N, int num_kb, int64_t tiles_m, int64
 
 // Launch with programmatic stream serialization and, for pairs, 2-CTA clusters; the
 // persistent grid is as many units as can be resident at once.
-template <bool RAW, bool PAIR, int OUT, bool MIXED>
+template <bool RAW, bool PAIR, int OUT, bool MIXED, bool SPLIT>
 static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                                  const gemm::Args& a, const DeviceInfo& dev, cudaStream_t s)
 {
     using namespace gemm;
-    cudaError_t e = ensure_smem_attr<RAW, PAIR, OUT, MIXED>(dev.device);
+    cudaError_t e = ensure_smem_attr<RAW, PAIR, OUT, MIXED, SPLIT>(dev.device);
     if (e != cudaSuccess)
         return e;
     int64_t resident = 0;
@@ -942,7 +954,7 @@ static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB,
     cudaLaunchConfig_t cfg = make_config(PAIR, Mode<PAIR>::SMEM_BYTES, s, attr);
     const int64_t units = std::min<int64_t>(a.num_items, resident);
     cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units));
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR, OUT, MIXED>, tmA, tmB, tmY, a);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT>, tmA, tmB, tmY, a);
 }
 
 // A 64-bit tag no earlier launch of this process used (high-entropy start, so slots
@@ -983,8 +995,8 @@ cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, bool mixed, const DeviceI
     return cudaSuccess;
 }
 
-// The dequant kernels by output type and tile mode.
-template <bool MIXED>
+// The dequant kernels by output type, tile mode and K-split.
+template <bool MIXED, bool SPLIT>
 static cudaError_t launch_dequant(bool pair, int out_dtype, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   const CUtensorMap& tmY, const gemm::Args& a, const DeviceInfo& dev,
                                   cudaStream_t s)
@@ -992,14 +1004,14 @@ static cudaError_t launch_dequant(bool pair, int out_dtype, const CUtensorMap& t
     using namespace gemm;
     switch (out_dtype) {
     case kOutF16:
-        return pair ? launch_kernel<false, true, kOutF16, MIXED>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<false, false, kOutF16, MIXED>(tmA, tmB, tmY, a, dev, s);
+        return pair ? launch_kernel<false, true, kOutF16, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutF16, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s);
     case kOutF32:
-        return pair ? launch_kernel<false, true, kOutF32, MIXED>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<false, false, kOutF32, MIXED>(tmA, tmB, tmY, a, dev, s);
+        return pair ? launch_kernel<false, true, kOutF32, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutF32, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s);
     default:
-        return pair ? launch_kernel<false, true, kOutBf16, MIXED>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<false, false, kOutBf16, MIXED>(tmA, tmB, tmY, a, dev, s);
+        return pair ? launch_kernel<false, true, kOutBf16, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutBf16, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s);
     }
 }
 
@@ -1072,12 +1084,19 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.b, p.K, p.N, (uint64_t)p.K * 2, BK, a.bn / 2,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
         return cudaErrorInvalidValue;
-    if (raw)
-        return pair ? launch_kernel<true, true, kOutBf16, false>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<true, false, kOutBf16, false>(tmA, tmB, tmY, a, dev, s);
+    const bool split = a.split > 1;  // never for the 16-bit path (planned without)
+    if (raw) {
+        if (split)
+            return pair ? launch_kernel<true, true, kOutBf16, false, true>(tmA, tmB, tmY, a, dev, s)
+                        : launch_kernel<true, false, kOutBf16, false, true>(tmA, tmB, tmY, a, dev, s);
+        return pair ? launch_kernel<true, true, kOutBf16, false, false>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<true, false, kOutBf16, false, false>(tmA, tmB, tmY, a, dev, s);
+    }
     if (p.mixed)
-        return launch_dequant<true>(pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
-    return launch_dequant<false>(pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
+        return launch_dequant<true, false>(pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
+    if (split)
+        return launch_dequant<false, true>(pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
+    return launch_dequant<false, false>(pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
 }
 
 cudaError_t read_device_error(unsigned int* value, bool clear)
