@@ -260,9 +260,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 // sub-partition as well).
 // MIXED: 16-bit activations times int8 weight codes (both bf16 operands), the fp32
 // accumulation over all of K kept in TMEM, epilogue (sum * w_scale) + bias.
-// SPLIT: the launch splits its last partial wave along K (the code for it lives only in
-// these instances, so the common kernel keeps its own, smaller code).
-template <bool RAW, bool PAIR, int OUT, bool MIXED, bool SPLIT>
+// SPLIT: the launch splits its last partial wave along K; RES: a residual is added.
+// Both live only in their own instances: unused code in the common kernel measurably
+// slowed it (instruction fetch on the first tile, register allocation).
+template <bool RAW, bool PAIR, int OUT, bool MIXED, bool SPLIT, bool RES>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const Args args)
@@ -629,7 +630,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                         // this lane's residual: 16 bytes of its own row (the element it writes)
                         float rv[PC];
-                        if (args.residual != nullptr && row < args.M && col < args.N) {
+                        if (RES && row < args.M && col < args.N) {
                             const uint4 rr = __ldcg(reinterpret_cast<const uint4*>(
                                 static_cast<const uint8_t*>(args.residual) + (row * args.N + col) * OT::BYTES));
                             unpack_out<OUT>(rr, rv);
@@ -650,7 +651,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             t[i] = __fmul_rn(t[i], wsv[i]);
                             if (args.bias)
                                 t[i] = __fadd_rn(t[i], bv[i]);
-                            if (args.residual)
+                            if (RES)
                                 t[i] = __fadd_rn(t[i], rv[i]);
                         }
                         uint32_t packed[4];
@@ -765,7 +766,7 @@ static bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ba
     return true;
 }
 
-template <bool RAW, bool PAIR, int OUT, bool MIXED, bool SPLIT>
+template <bool RAW, bool PAIR, int OUT, bool MIXED, bool SPLIT, bool RES>
 static cudaError_t ensure_smem_attr(int device)
 {
     static bool done[64] = {};
@@ -773,7 +774,7 @@ static cudaError_t ensure_smem_attr(int device)
     std::lock_guard<std::mutex> lock(mu);
     if (device >= 0 && device < 64 && done[device])
         return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT>,
+    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT, RES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)gemm::Mode<PAIR>::SMEM_BYTES);
     if (e == cudaSuccess) {
@@ -781,7 +782,7 @@ static cudaError_t ensure_smem_attr(int device)
         // with (registers are granted per warp in units of 8 per thread), else the
         // epilogue's increase would wait forever: refuse to launch instead
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT>);
+        e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT, RES>);
         if (e == cudaSuccess &&
             (uint64_t)((fa.numRegs + 7) / 8 * 8) * gemm::THREADS < (uint64_t)gemm::REGS_NEEDED_PER_BLOCK)
             e = cudaErrorInvalidConfiguration;
@@ -822,13 +823,14 @@ static cudaError_t resident_units(const DeviceInfo& dev, int64_t* out)
     std::lock_guard<std::mutex> lock(mu);
     int& n = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
     if (n == 0) {
-        cudaError_t e = ensure_smem_attr<false, true, gemm::kOutBf16, false, false>(dev.device);
+        cudaError_t e = ensure_smem_attr<false, true, gemm::kOutBf16, false, false, false>(dev.device);
         if (e != cudaSuccess)
             return e;
         cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = make_config(true, gemm::Mode<true>::SMEM_BYTES, nullptr, attr);
         cfg.gridDim = dim3(2 * (dev.sm_count / 2));
-        e = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_kernel<false, true, gemm::kOutBf16, false, false>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_kernel<false, true, gemm::kOutBf16, false, false, false>,
+                                           &cfg);
         if (e != cudaSuccess)
             return e;
         if (n <= 0)
@@ -939,12 +941,12 @@ static void choose_tile(int64_t M, int64_t N, int num_kb, int64_t tiles_m, int64
 
 // Launch with programmatic stream serialization and, for pairs, 2-CTA clusters; the
 // persistent grid is as many units as can be resident at once.
-template <bool RAW, bool PAIR, int OUT, bool MIXED, bool SPLIT>
+template <bool RAW, bool PAIR, int OUT, bool MIXED, bool SPLIT, bool RES>
 static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                                  const gemm::Args& a, const DeviceInfo& dev, cudaStream_t s)
 {
     using namespace gemm;
-    cudaError_t e = ensure_smem_attr<RAW, PAIR, OUT, MIXED, SPLIT>(dev.device);
+    cudaError_t e = ensure_smem_attr<RAW, PAIR, OUT, MIXED, SPLIT, RES>(dev.device);
     if (e != cudaSuccess)
         return e;
     int64_t resident = 0;
@@ -954,7 +956,7 @@ static cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmB,
     cudaLaunchConfig_t cfg = make_config(PAIR, Mode<PAIR>::SMEM_BYTES, s, attr);
     const int64_t units = std::min<int64_t>(a.num_items, resident);
     cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units));
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT>, tmA, tmB, tmY, a);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT, RES>, tmA, tmB, tmY, a);
 }
 
 // A 64-bit tag no earlier launch of this process used (high-entropy start, so slots
@@ -995,8 +997,8 @@ cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, bool mixed, const DeviceI
     return cudaSuccess;
 }
 
-// The dequant kernels by output type, tile mode and K-split.
-template <bool MIXED, bool SPLIT>
+// The dequant kernels by output type, tile mode, K-split and residual.
+template <bool MIXED, bool SPLIT, bool RES>
 static cudaError_t launch_dequant(bool pair, int out_dtype, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   const CUtensorMap& tmY, const gemm::Args& a, const DeviceInfo& dev,
                                   cudaStream_t s)
@@ -1004,15 +1006,24 @@ static cudaError_t launch_dequant(bool pair, int out_dtype, const CUtensorMap& t
     using namespace gemm;
     switch (out_dtype) {
     case kOutF16:
-        return pair ? launch_kernel<false, true, kOutF16, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<false, false, kOutF16, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s);
+        return pair ? launch_kernel<false, true, kOutF16, MIXED, SPLIT, RES>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutF16, MIXED, SPLIT, RES>(tmA, tmB, tmY, a, dev, s);
     case kOutF32:
-        return pair ? launch_kernel<false, true, kOutF32, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<false, false, kOutF32, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s);
+        return pair ? launch_kernel<false, true, kOutF32, MIXED, SPLIT, RES>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutF32, MIXED, SPLIT, RES>(tmA, tmB, tmY, a, dev, s);
     default:
-        return pair ? launch_kernel<false, true, kOutBf16, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<false, false, kOutBf16, MIXED, SPLIT>(tmA, tmB, tmY, a, dev, s);
+        return pair ? launch_kernel<false, true, kOutBf16, MIXED, SPLIT, RES>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<false, false, kOutBf16, MIXED, SPLIT, RES>(tmA, tmB, tmY, a, dev, s);
     }
+}
+
+template <bool MIXED, bool SPLIT>
+static cudaError_t launch_dequant(bool res, bool pair, int out_dtype, const CUtensorMap& tmA,
+                                  const CUtensorMap& tmB, const CUtensorMap& tmY, const gemm::Args& a,
+                                  const DeviceInfo& dev, cudaStream_t s)
+{
+    return res ? launch_dequant<MIXED, SPLIT, true>(pair, out_dtype, tmA, tmB, tmY, a, dev, s)
+               : launch_dequant<MIXED, SPLIT, false>(pair, out_dtype, tmA, tmB, tmY, a, dev, s);
 }
 
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why)
@@ -1087,16 +1098,17 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     const bool split = a.split > 1;  // never for the 16-bit path (planned without)
     if (raw) {
         if (split)
-            return pair ? launch_kernel<true, true, kOutBf16, false, true>(tmA, tmB, tmY, a, dev, s)
-                        : launch_kernel<true, false, kOutBf16, false, true>(tmA, tmB, tmY, a, dev, s);
-        return pair ? launch_kernel<true, true, kOutBf16, false, false>(tmA, tmB, tmY, a, dev, s)
-                    : launch_kernel<true, false, kOutBf16, false, false>(tmA, tmB, tmY, a, dev, s);
+            return pair ? launch_kernel<true, true, kOutBf16, false, true, false>(tmA, tmB, tmY, a, dev, s)
+                        : launch_kernel<true, false, kOutBf16, false, true, false>(tmA, tmB, tmY, a, dev, s);
+        return pair ? launch_kernel<true, true, kOutBf16, false, false, false>(tmA, tmB, tmY, a, dev, s)
+                    : launch_kernel<true, false, kOutBf16, false, false, false>(tmA, tmB, tmY, a, dev, s);
     }
+    const bool res = p.residual != nullptr;
     if (p.mixed)
-        return launch_dequant<true, false>(pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
+        return launch_dequant<true, false>(res, pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
     if (split)
-        return launch_dequant<false, true>(pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
-    return launch_dequant<false, false>(pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
+        return launch_dequant<false, true>(res, pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
+    return launch_dequant<false, false>(res, pair, p.out_dtype, tmA, tmB, tmY, a, dev, s);
 }
 
 cudaError_t read_device_error(unsigned int* value, bool clear)
