@@ -20,7 +20,7 @@ LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libck_int8.so")
 
 SOURCES = ["api.cu", "quantize.cu", "gemm.cu"]
-HEADERS = ["ck_device.cuh", "ck_internal.h"]
+HEADERS = ["ck_device.cuh", "ck_internal.h", "gemm_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

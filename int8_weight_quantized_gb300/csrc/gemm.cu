@@ -55,6 +55,7 @@
 
 #include "ck_device.cuh"
 #include "ck_internal.h"
+#include "gemm_common.cuh"
 
 namespace ck {
 
@@ -79,12 +80,9 @@ constexpr uint32_t REGS_NEEDED_PER_BLOCK = 128 * REGS_WG0 + 256 * REGS_EPI;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr int B_BOX_ROWS = BN / 2;                       // most weight rows per TMA box
 constexpr uint32_t B_BOX_BYTES = B_BOX_ROWS * BK * 2;
-constexpr uint32_t OUT_ROW_BYTES = 64;                   // a TMA store box is 32 rows x 64 bytes
-constexpr uint32_t OUT_BUF_BYTES = 32 * OUT_ROW_BYTES;
 constexpr uint32_t OUT_BYTES = EPI_WARPS * 2 * OUT_BUF_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t BAR_BYTES = 256;
-constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull;   // 2 s per wait
 
 // Per-mode shapes: a pair CTA stages 128 weight rows per k-block, a single CTA 256.
 template <bool PAIR>
@@ -187,71 +185,6 @@ __device__ __forceinline__ void unit_coords(int64_t u, const Args& a, int& um, i
     const int64_t r = u - g * per_group;
     um = (int)(first + r % rows);
     nb = (int)(r / rows);
-}
-
-// Bounded wait used during teardown only (never raises the abort flag again).
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
-                                           uint64_t timeout_ns)
-{
-    if (mbar_try_wait(bar, parity))
-        return;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity))
-            return;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
-            atomicOr(err, kErrWaitDrain);
-            return;
-        }
-    }
-}
-
-// Output element types of the epilogue (the pages' int8_linear(..., out_dtype)).
-enum : int { kOutBf16 = 0, kOutF16 = 1, kOutF32 = 2 };
-
-template <int OUT>
-struct OutType {
-    static constexpr int BYTES = OUT == kOutF32 ? 4 : 2;
-    static constexpr int BOX_COLS = (int)OUT_ROW_BYTES / BYTES;  // 32 (16-bit types) or 16 (fp32)
-    static constexpr int PER_CHUNK = 16 / BYTES;                   // values per 16-byte chunk
-};
-
-// 16 bytes of output-type values -> fp32 (exact).
-template <int OUT>
-__device__ __forceinline__ void unpack_out(const uint4& r, float (&v)[OutType<OUT>::PER_CHUNK])
-{
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-    if (OUT == kOutF32) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            v[i] = __uint_as_float(w[i]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (OUT == kOutF16) {
-                const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-                v[2 * i] = __low2float(h);
-                v[2 * i + 1] = __high2float(h);
-            } else {
-                const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-                v[2 * i] = __low2float(h);
-                v[2 * i + 1] = __high2float(h);
-            }
-        }
-    }
-}
-
-// Round two fp32 values to the output type and pack them (lower column first).
-template <int OUT>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi)
-{
-    if (OUT == kOutF16) {
-        __half2 v = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&v);
-    } else {
-        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&v);
-    }
 }
 
 // 12 warps put three warps on each of the four SM sub-partitions, whose register files
@@ -741,9 +674,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // 2-D row-major tensor of `rows` x `cols` elements with a row pitch of `pitch_bytes`.
-static bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
-                        uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz,
-                        std::string* why)
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                 uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz, std::string* why)
 {
     auto fn = encode_fn();
     if (!fn) {
