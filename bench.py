@@ -44,7 +44,8 @@ DEFAULT_WORKLOAD = synthetic.TENSORWISE_4096[0]
 FLUSH_BYTES = 512 << 20  # > 129 MB of L2: written between steps (outside the timed events)
 CLEAN_BYTES = 256 << 20  # then read, so the step does not start by writing back the flush's dirty lines
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
-GEMM_SOURCES = ["int8_weight_quantized_gb300/csrc/gemm.cu", "int8_weight_quantized_gb300/csrc/ck_device.cuh"]
+GEMM_SOURCES = ["int8_weight_quantized_gb300/csrc/gemm.cu", "int8_weight_quantized_gb300/csrc/ck_device.cuh",
+                "int8_weight_quantized_gb300/csrc/gemm_common.cuh"]
 
 
 # ---------------------------------------------------------------- helpers
