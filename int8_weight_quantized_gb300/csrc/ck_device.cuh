@@ -367,6 +367,39 @@ __device__ __forceinline__ void tmem_wait_ld()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// The four MMAs of one 64-deep k-block in one statement: A and B descriptors advance by
+// 32 bytes (2 in the address field) per 16-element K step.  The first MMA adds to D only
+// if `accumulate`; the other three always do.  PAIR: cta_group::2 (issued by the leader).
+template <bool PAIR>
+__device__ __forceinline__ void mma_bf16_kblock(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate)
+{
+    if (PAIR)
+        asm volatile(
+            "{\n\t.reg .pred p, t;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "setp.eq.b32 t, %4, %4;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %5, %6, %3, t;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %7, %8, %3, t;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %9, %10, %3, t;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "l"(a_desc + 2), "l"(b_desc + 2),
+            "l"(a_desc + 4), "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p, t;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "setp.eq.b32 t, %4, %4;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, t;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, t;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, t;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "l"(a_desc + 2), "l"(b_desc + 2),
+            "l"(a_desc + 4), "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6)
+            : "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with
 // 128-byte swizzling: rows of 128 bytes (64 bf16 along K), 8-row swizzle atoms of
 // 1024 bytes stacked along M/N.  Fields: start address >> 4 (bits 0-13), leading

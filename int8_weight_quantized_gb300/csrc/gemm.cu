@@ -67,6 +67,7 @@ constexpr int BM = 128;       // rows of a CTA's tile (a pair covers 2 * BM)
 constexpr int BN = 256;       // widest tile; a launch may use any multiple of 32 up to it
 constexpr int BK = 64;        // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;    // K per kind::f16 instruction
+static_assert(BK / UMMA_K == 4, "mma_bf16_kblock issues the four MMAs of a k-block");
 constexpr int CHUNK_KB = 16;  // k-blocks per exact fp32 chunk (16 * 64 = 1024 products)
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 4;                  // warps 0-3: producer, MMA issuer, two idle
@@ -323,36 +324,35 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t phase = 0;
                 uint32_t acc_iter = 0;
                 bool ok = true;
+                // One thread issues every MMA, so its loop is kept short: the invariants live
+                // in registers and a stage's descriptors are stage 0's plus an offset in the
+                // address field (shared addresses >> 4 stay below 2^14: no carry leaves it).
+                const uint32_t idesc = args.idesc;
+                const int chunk_kb = args.chunk_kb;
+                const uint64_t timeout_ns = args.timeout_ns;
+                const uint64_t desc_a0 = desc_kmajor_sw128(smem_u32(s_ab));
+                constexpr uint64_t kDescStage = MD::STAGE_BYTES >> 4;
+                constexpr uint64_t kDescB = A_BYTES >> 4;
                 for (int64_t it = cluster; ok && it < args.num_items; it += clusters) {
                     const Item w = item_of<SPLIT>(it, args);
-                    for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += args.chunk_kb) {
+                    for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += chunk_kb) {
                         const uint32_t buf = acc_iter & 1u;
                         const uint32_t acc_phase = (acc_iter >> 1) & 1u;
-                        if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort_flag, err, kErrWaitMma, args.timeout_ns)) {
+                        if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort_flag, err, kErrWaitMma, timeout_ns)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint32_t d_tmem = tmem_base + buf * BN;
-                        const int kend = min(kb0 + args.chunk_kb, w.kb_end);
+                        const int kend = min(kb0 + chunk_kb, w.kb_end);
                         for (int kb = kb0; kb < kend; ++kb) {
-                            if (!mbar_wait(&full[stage], phase, abort_flag, err, kErrWaitMma, args.timeout_ns)) {
+                            if (!mbar_wait(&full[stage], phase, abort_flag, err, kErrWaitMma, timeout_ns)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t a0 = smem_u32(s_ab + (size_t)stage * MD::STAGE_BYTES);
-                            const uint32_t b0 = a0 + A_BYTES;
-    #pragma unroll
-                            for (int k = 0; k < BK / UMMA_K; ++k) {
-                                // +32 bytes per 16-element K step inside the 128-byte swizzle row
-                                const uint64_t ad = desc_kmajor_sw128(a0 + k * 32), bd = desc_kmajor_sw128(b0 + k * 32);
-                                const uint32_t accumulate = (kb > kb0 || k > 0) ? 1u : 0u;
-                                if (PAIR)
-                                    mma_bf16_pair(d_tmem, ad, bd, args.idesc, accumulate);
-                                else
-                                    mma_bf16(d_tmem, ad, bd, args.idesc, accumulate);
-                            }
+                            const uint64_t ad = desc_a0 + (uint64_t)stage * kDescStage;
+                            mma_bf16_kblock<PAIR>(d_tmem, ad, ad + kDescB, idesc, kb > kb0 ? 1u : 0u);
                             if (PAIR)
                                 mma_commit_pair(&empty[stage], kPairMask);  // frees the stage in both CTAs
                             else
@@ -402,11 +402,34 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int64_t row = m0 + quarter * 32 + lane;
             const int64_t cbase = n0 + half * 128;
             float xsv = 0.0f, ws_scalar = 0.0f;
+            // w_scale and bias of columns cbase + 4 lane .. + 3 (0 past the tile or N); the store
+            // loop takes a column's values from its lane by shuffle.  Loaded here, they are in
+            // flight during the K loop: loaded per chunk in the store loop, their latency held
+            // up every tile's stores, ~4 us per launch at 4096^3 (the last tile's is exposed).
+            float wsr[4] = {0.0f, 0.0f, 0.0f, 0.0f}, bsr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             if (!RAW) {  // the scalar scales and this lane's row scale, in flight during the K loop
                 if (args.scalar_scales)
                     ws_scalar = __ldg(args.ws);
                 if (!MIXED)
                     xsv = args.scalar_scales ? __ldg(args.xs) : (row < args.M ? __ldg(args.xs + row) : 0.0f);
+                const int64_t c4 = cbase + 4 * lane;
+                if (4 * lane < ncols && c4 < args.N) {  // N % 8 == 0: a group of 4 is all in or all out
+                    if (!args.scalar_scales) {
+                        const float4 w4 = __ldg(reinterpret_cast<const float4*>(args.ws + c4));
+                        wsr[0] = w4.x;
+                        wsr[1] = w4.y;
+                        wsr[2] = w4.z;
+                        wsr[3] = w4.w;
+                    }
+                    if (args.bias) {
+                        const uint2 braw = __ldg(reinterpret_cast<const uint2*>(args.bias + c4));
+                        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&braw);
+                        bsr[0] = __low2float(b2[0]);
+                        bsr[1] = __high2float(b2[0]);
+                        bsr[2] = __low2float(b2[1]);
+                        bsr[3] = __high2float(b2[1]);
+                    }
+                }
             }
             int32_t run[128];
 #pragma unroll
@@ -532,34 +555,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const int64_t col = col0 + c * PC;
                         // the same columns for every lane: broadcast loads, L1 hits after the
                         // first tile of a column range
+                        // the columns' w_scale and bias from the lanes that loaded them (columns
+                        // past N hold 0: computed, then clipped by the store)
                         float wsv[PC], bv[PC];
-                        if (col < args.N) {  // N % 8 == 0: a chunk is all in or all out
+                        const int src = (g * OT::BOX_COLS + c * PC) >> 2;
 #pragma unroll
-                            for (int h = 0; h < PC / 4; ++h) {
-                                if (args.scalar_scales) {
-                                    wsv[4 * h] = wsv[4 * h + 1] = wsv[4 * h + 2] = wsv[4 * h + 3] = ws_scalar;
-                                } else {
-                                    const float4 w4 = __ldg(reinterpret_cast<const float4*>(args.ws + col + 4 * h));
-                                    wsv[4 * h] = w4.x;
-                                    wsv[4 * h + 1] = w4.y;
-                                    wsv[4 * h + 2] = w4.z;
-                                    wsv[4 * h + 3] = w4.w;
-                                }
-                                if (args.bias) {
-                                    const uint2 braw = __ldg(reinterpret_cast<const uint2*>(args.bias + col + 4 * h));
-                                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&braw);
-                                    bv[4 * h] = __low2float(b2[0]);
-                                    bv[4 * h + 1] = __high2float(b2[0]);
-                                    bv[4 * h + 2] = __low2float(b2[1]);
-                                    bv[4 * h + 3] = __high2float(b2[1]);
-                                } else {
-                                    bv[4 * h] = bv[4 * h + 1] = bv[4 * h + 2] = bv[4 * h + 3] = 0.0f;
-                                }
-                            }
-                        } else {  // past the last column: computed, then clipped by the store
-#pragma unroll
-                            for (int i = 0; i < PC; ++i)
-                                wsv[i] = bv[i] = 0.0f;
+                        for (int i = 0; i < PC; ++i) {
+                            wsv[i] = args.scalar_scales ? ws_scalar : __shfl_sync(0xffffffffu, wsr[i & 3], src + (i >> 2));
+                            bv[i] = __shfl_sync(0xffffffffu, bsr[i & 3], src + (i >> 2));
                         }
                         // this lane's residual: 16 bytes of its own row (the element it writes)
                         float rv[PC];
