@@ -272,17 +272,6 @@ __device__ __forceinline__ void tc_fence_after()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16/f16 inputs, fp32 accum).
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this thread
 // has completed.
@@ -313,18 +302,6 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// D (rows in both CTAs' TMEM) (+)= A (rows split over both CTAs) * B (N split over both
-// CTAs)^T; issued by one thread of the pair's leader CTA.
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 
 // Arrive once on the barrier at the offset of `bar` in every CTA named in cta_mask when
 // the pair MMAs issued so far by this thread have completed.
@@ -367,9 +344,12 @@ __device__ __forceinline__ void tmem_wait_ld()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// The four MMAs of one 64-deep k-block in one statement: A and B descriptors advance by
-// 32 bytes (2 in the address field) per 16-element K step.  The first MMA adds to D only
-// if `accumulate`; the other three always do.  PAIR: cta_group::2 (issued by the leader).
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T over one 64-deep k-block, kind::f16 (bf16
+// or f16 inputs, fp32 accumulator): four MMAs in one statement, the A and B descriptors
+// advancing by 32 bytes (2 in the address field) per 16-element K step.  The first MMA
+// adds to D only if `accumulate`; the other three always do.  PAIR: cta_group::2, issued
+// by one thread of the pair's leader CTA; D's rows are in both CTAs' TMEM, A's rows are
+// split over both CTAs' shared memory and so are B's (N).
 template <bool PAIR>
 __device__ __forceinline__ void mma_bf16_kblock(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                 uint32_t accumulate)
