@@ -785,6 +785,13 @@ static int64_t kblock_cost(bool pair, int bn)
     return pair ? 30500 + 15 * (int64_t)bn : 30000 + 29 * (int64_t)bn;
 }
 
+// A launch of CTA pairs costs about 3 us more than one of single CTAs (2-CTA cluster
+// launch and set-up, the pair's longer last epilogue): on GB300, single CTAs finished
+// one-wave problems (1024x4096x4096, 274x2048x2048) ~2 us sooner at the same tile width,
+// where the per-k-block costs above predict the opposite.  The term only decides
+// problems of one or two waves.
+constexpr int64_t kPairLaunchCost = 300000;
+
 // A K-split tail slice must keep at least this many k-blocks.  Publishing the slices'
 // sums (write, fence, count the arrival) and adding them in the last slice cost, as
 // measured on GB300 (2-, 3- and 4-way splits of 64- and 48-k-block units), about
@@ -821,7 +828,7 @@ static TileCost tile_cost(bool pair, int bn, int64_t units, int64_t resident, in
             }
         }
     }
-    c.cost *= kblock_cost(pair, bn);
+    c.cost = c.cost * kblock_cost(pair, bn) + (pair ? kPairLaunchCost : 0);
     return c;
 }
 
