@@ -65,10 +65,10 @@ namespace gemm {
 
 constexpr int BM = 128;       // rows of a CTA's tile (a pair covers 2 * BM)
 constexpr int BN = 256;       // widest tile; a launch may use any multiple of 32 up to it
-constexpr int BK = 64;        // one 128-byte swizzle row of bf16
+constexpr int BK = 64;        // one 128-byte swizzle row of bf16: the width of every TMA box
 constexpr int UMMA_K = 16;    // K per kind::f16 instruction
-static_assert(BK / UMMA_K == 4, "mma_bf16_kblock issues the four MMAs of a k-block");
-constexpr int CHUNK_KB = 16;  // k-blocks per exact fp32 chunk (16 * 64 = 1024 products)
+static_assert(BK / UMMA_K == 4, "mma_bf16_kblock issues the four MMAs of a 64-deep sub-block");
+constexpr int CHUNK_K = 1024; // products per exact fp32 chunk
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 4;                  // warps 0-3: producer, MMA issuer, two idle
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
@@ -85,12 +85,21 @@ constexpr uint32_t OUT_BYTES = EPI_WARPS * 2 * OUT_BUF_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t BAR_BYTES = 256;
 
-// Per-mode shapes: a pair CTA stages 128 weight rows per k-block, a single CTA 256.
+// Per-mode shapes: a pair CTA stages 128 weight rows per 64-deep sub-block, a single CTA
+// 256.  A pipeline stage (k-block) holds KSUB sub-blocks: every stage costs a fixed
+// hand-off (barriers, loads, commit) that 64-deep stages could not hide -- a unit's
+// k-block took ~305 ns however narrow the tile; CTA pairs stage 128-deep k-blocks (three
+// stages), 4096^3 went from 96 to 80 us.  Single CTAs stage twice the weight rows, so a
+// 128-deep stage leaves them two stages, which was slower: they keep 64-deep ones.
 template <bool PAIR>
 struct Mode {
-    static constexpr uint32_t B_BYTES = PAIR ? B_BOX_BYTES : 2 * B_BOX_BYTES;
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int KSUB = PAIR ? 2 : 1;
+    static constexpr int KB = BK * KSUB;                  // K per k-block
+    static constexpr int CHUNK_KB = CHUNK_K / KB;         // k-blocks per exact fp32 chunk
+    static constexpr uint32_t B_BYTES = PAIR ? B_BOX_BYTES : 2 * B_BOX_BYTES;  // per sub-block
+    // a stage: the KSUB A sub-blocks, then the KSUB B sub-blocks
+    static constexpr uint32_t STAGE_BYTES = KSUB * (A_BYTES + B_BYTES);
+    static constexpr int STAGES = PAIR ? 3 : 4;
     static constexpr uint32_t IDESC_M = PAIR ? idesc_bf16_f32<2 * BM, 0>() : idesc_bf16_f32<BM, 0>();
     static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -111,7 +120,7 @@ struct Args {
     uint32_t tx_bytes;      // bytes of one k-block counted on the (leader's) full barrier
     int units_m, tiles_m, tiles_n, num_kb, group_m;
     int scalar_scales;
-    int chunk_kb;           // k-blocks per TMEM accumulation: CHUNK_KB (exact), all of K (16-bit activations)
+    int chunk_kb;           // k-blocks per TMEM accumulation: 1024 products (exact), all of K (16-bit activations)
     uint64_t timeout_ns;
     // K-split of the last partial wave: units [full_units, num_units) are each computed
     // as `split` K-slices by different units of the grid; every slice writes its int32
@@ -286,19 +295,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                             break;
                         }
                         uint8_t* sa = s_ab + (size_t)stage * MD::STAGE_BYTES;
-                        uint8_t* sb = sa + A_BYTES;
+                        uint8_t* sb = sa + MD::KSUB * A_BYTES;
                         if (PAIR) {
                             // both CTAs' bytes are counted on the leader's barrier
                             const uint32_t bar = mapa_shared(&full[stage], 0);
                             if (leader)
                                 mbar_arrive_expect_tx(&full[stage], args.tx_bytes);
-                            tma_load_2d_pair(sa, &tmA, bar, kb * BK, m0);
-                            tma_load_2d_pair(sb, &tmB, bar, kb * BK, n0 + rank * half_rows);
+#pragma unroll
+                            for (int sub = 0; sub < MD::KSUB; ++sub) {
+                                const int32_t k0 = kb * MD::KB + sub * BK;
+                                tma_load_2d_pair(sa + sub * A_BYTES, &tmA, bar, k0, m0);
+                                tma_load_2d_pair(sb + sub * MD::B_BYTES, &tmB, bar, k0, n0 + rank * half_rows);
+                            }
                         } else {
                             mbar_arrive_expect_tx(&full[stage], args.tx_bytes);
-                            tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
-                            tma_load_2d(sb, &tmB, &full[stage], kb * BK, n0);
-                            tma_load_2d(sb + half_rows * BK * 2, &tmB, &full[stage], kb * BK, n0 + half_rows);
+#pragma unroll
+                            for (int sub = 0; sub < MD::KSUB; ++sub) {
+                                const int32_t k0 = kb * MD::KB + sub * BK;
+                                uint8_t* b = sb + sub * MD::B_BYTES;
+                                tma_load_2d(sa + sub * A_BYTES, &tmA, &full[stage], k0, m0);
+                                tma_load_2d(b, &tmB, &full[stage], k0, n0);
+                                tma_load_2d(b + half_rows * BK * 2, &tmB, &full[stage], k0, n0 + half_rows);
+                            }
                         }
                         issued_mask |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -332,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint64_t timeout_ns = args.timeout_ns;
                 const uint64_t desc_a0 = desc_kmajor_sw128(smem_u32(s_ab));
                 constexpr uint64_t kDescStage = MD::STAGE_BYTES >> 4;
-                constexpr uint64_t kDescB = A_BYTES >> 4;
+                constexpr uint64_t kDescB = (MD::KSUB * A_BYTES) >> 4;
                 for (int64_t it = cluster; ok && it < args.num_items; it += clusters) {
                     const Item w = item_of<SPLIT>(it, args);
                     for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += chunk_kb) {
@@ -352,7 +370,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                             }
                             tc_fence_after();
                             const uint64_t ad = desc_a0 + (uint64_t)stage * kDescStage;
-                            mma_bf16_kblock<PAIR>(d_tmem, ad, ad + kDescB, idesc, kb > kb0 ? 1u : 0u);
+#pragma unroll
+                            for (int sub = 0; sub < MD::KSUB; ++sub)
+                                mma_bf16_kblock<PAIR>(d_tmem, ad + sub * (A_BYTES >> 4),
+                                                      ad + kDescB + sub * (MD::B_BYTES >> 4), idesc,
+                                                      (kb > kb0 || sub > 0) ? 1u : 0u);
                             if (PAIR)
                                 mma_commit_pair(&empty[stage], kPairMask);  // frees the stage in both CTAs
                             else
@@ -775,22 +797,21 @@ static cudaError_t resident_units(const DeviceInfo& dev, int64_t* out)
     return cudaSuccess;
 }
 
-// Time of one 64-deep k-block of one unit, in units of 0.01 ns, as measured on GB300
-// over tile widths 32..256 (25900x16384x4096, many waves): a CTA pair's 256-row unit
-// takes about 305 + 0.15 * bn ns, a single CTA's 128-row unit about 300 + 0.29 * bn ns.
-// Narrow tiles hardly save time per k-block (the MMA chain has a latency floor near the
-// 256-wide tile's throughput time), so the width mainly trades wave quantization.
+// Time of 64 deep of K of one unit, in units of 0.01 ns, as measured on GB300 over tile
+// widths 32..256 (25900x16384x4096, many waves): a CTA pair's 256-row unit (128-deep
+// stages) takes about 218 + 0.41 * bn ns, a single CTA's 128-row unit (64-deep stages)
+// about 295 + 0.35 * bn ns.  Narrow tiles save little per k-block, so the width mainly
+// trades wave quantization.
 static int64_t kblock_cost(bool pair, int bn)
 {
-    return pair ? 30500 + 15 * (int64_t)bn : 30000 + 29 * (int64_t)bn;
+    return pair ? 21800 + 41 * (int64_t)bn : 29500 + 35 * (int64_t)bn;
 }
 
-// A launch of CTA pairs costs about 3 us more than one of single CTAs (2-CTA cluster
-// launch and set-up, the pair's longer last epilogue): on GB300, single CTAs finished
-// one-wave problems (1024x4096x4096, 274x2048x2048) ~2 us sooner at the same tile width,
-// where the per-k-block costs above predict the opposite.  The term only decides
-// problems of one or two waves.
-constexpr int64_t kPairLaunchCost = 300000;
+// A launch of CTA pairs costs about 2 us more than one of single CTAs (2-CTA cluster
+// launch and set-up, the pair's longer last epilogue): measured on a one-wave problem
+// (1024x4096x4096) as the launch time minus the k-block costs above, per mode.  The
+// term only decides problems of one or two waves.
+constexpr int64_t kPairLaunchCost = 210000;
 
 // A K-split tail slice must keep at least this many k-blocks.  Publishing the slices'
 // sums (write, fence, count the arrival) and adding them in the last slice cost, as
@@ -1002,9 +1023,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.residual = p.residual;
     a.acc = p.acc;
     a.tiles_m = (int)((p.M + BM - 1) / BM);
-    a.num_kb = (int)((p.K + BK - 1) / BK);
     a.scalar_scales = p.scalar_scales;
-    a.chunk_kb = p.mixed ? a.num_kb : CHUNK_KB;
     a.timeout_ns = DEFAULT_TIMEOUT_NS;
     GemmPlan plan;
     const cudaError_t e = plan_gemm(p.M, p.N, p.K, p.mixed, dev, &plan);
@@ -1033,7 +1052,10 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
         a.epoch = next_gemm_epoch();
     }
     a.idesc = (pair ? Mode<true>::IDESC_M : Mode<false>::IDESC_M) | ((uint32_t)(a.bn >> 3) << 17);
-    a.tx_bytes = (pair ? 2u : 1u) * (A_BYTES + (uint32_t)(pair ? a.bn / 2 : a.bn) * BK * 2);
+    const int kb_depth = pair ? Mode<true>::KB : Mode<false>::KB;  // K per k-block of this mode
+    a.num_kb = (int)((p.K + kb_depth - 1) / kb_depth);
+    a.chunk_kb = p.mixed ? a.num_kb : CHUNK_K / kb_depth;
+    a.tx_bytes = (pair ? 2u : 1u) * (uint32_t)(kb_depth / BK) * (A_BYTES + (uint32_t)(pair ? a.bn / 2 : a.bn) * BK * 2);
     if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.b, p.K, p.N, (uint64_t)p.K * 2, BK, a.bn / 2,
                      CU_TENSOR_MAP_SWIZZLE_128B, why))
         return cudaErrorInvalidValue;
