@@ -98,6 +98,20 @@ def test_s32_every_tile_width(monkeypatch, bn, pair):
     assert np.array_equal(gpu_acc(q, w), oracle.gemm_s32(q.numpy(), w.numpy()))
 
 
+@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("K", [16, 64, 80, 128, 144, 192, 1040])
+def test_s32_k_inside_and_across_stages(monkeypatch, K, pair):
+    """CTA pairs stage 128-deep k-blocks (two 64-deep boxes per operand), single CTAs
+    64-deep ones: K shorter than one box, than one stage, and ending inside a stage's first
+    or second box all give the exact accumulators (the boxes past K are zero-filled)."""
+    monkeypatch.setenv("CK_GEMM_PAIR", pair)
+    M, N = 300, 264
+    assert ck.ck_gemm_tile_config(M, N, K)[1] == (pair == "1")
+    q = synthetic.int8_uniform((M, K), seed=K + 11)
+    w = synthetic.int8_uniform((N, K), seed=K + 12)
+    assert np.array_equal(gpu_acc(q, w), oracle.gemm_s32(q.numpy(), w.numpy()))
+
+
 TYPED = [(torch.float16, oracle.OUT_F16), (torch.float32, oracle.OUT_F32), (torch.bfloat16, oracle.OUT_BF16)]
 
 
