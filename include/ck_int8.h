@@ -39,6 +39,14 @@
  *     (after the shape checks); the buffers sized by M may then be NULL.
  *   - Device: compute capability 10.3 (GB300) only, else CK_ERR_UNSUPPORTED_DEVICE.
  *     There is no fallback path of any kind.
+ *   - CUDA graphs: every entry point may be captured (cudaStreamBeginCapture) and the
+ *     graph replayed with new data in the same buffers; the results equal uncaptured
+ *     calls.  Make one uncaptured call per device first (it sets kernel attributes and
+ *     looks up the library's device symbols).  Under capture, ck_int8_linear in
+ *     tensorwise mode runs its quantize as two launches plus a separate weight widening
+ *     (the single launch exchanges block maxima under a per-call tag, which a replay would
+ *     repeat), and no GEMM splits its last wave along K (the split's arrival counters are
+ *     tagged the same way): same results, a few microseconds slower per call.
  */
 #ifndef CK_INT8_H
 #define CK_INT8_H

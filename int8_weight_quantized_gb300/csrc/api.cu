@@ -307,6 +307,20 @@ size_t ck_int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode)
     return linear_ws_bytes(M, N, K, mode, kMaxPartials);
 }
 
+// Whether work enqueued on `s` is being captured into a CUDA graph.  A captured launch
+// replays with the arguments it was captured with, so the per-launch tags that the
+// single-launch tensorwise preparation (block maxima exchanged in tagged slots) and the
+// GEMM's K-split tail (tagged arrival counters) take from the host would repeat on every
+// replay, and a replay could read the previous replay's maxima or miscount its arrivals.
+// Under capture the layer therefore uses forms without tags: the two-launch tensorwise
+// quantize (per-block maxima, then a pass that reduces them), a separate weight widening,
+// and no K-split.
+static bool stream_capturing(cudaStream_t s)
+{
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    return cudaStreamIsCapturing(s, &st) == cudaSuccess && st != cudaStreamCaptureStatusNone;
+}
+
 static bool valid_out_dtype(int t)
 {
     return t == CK_OUT_BF16 || t == CK_OUT_F16 || t == CK_OUT_F32;
@@ -347,8 +361,15 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
     log_shape("int8_linear", M, N, K, mode, "prep(1 launch) + tcgen05 bf16-exact GEMM, 2-CTA 256x256 tiles");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     LinearWorkspace ws = carve_linear(workspace, M, N, K, mode);
+    const bool graph = stream_capturing(s);
     cudaError_t e;
-    {
+    if (mode == CK_TENSORWISE && graph) {
+        // captured: per-block maxima, a quantize pass that reduces them, the widening apart
+        ProfScope ps(kProfQuantize, 2, s);
+        e = launch_quantize_tensorwise(x, M, K, nullptr, ws.a16, ws.xs, static_cast<float*>(ws.scratch), dev, s);
+        if (e == cudaSuccess)
+            e = launch_widen_int8(w, ws.b16, N * K, dev, s);
+    } else {
         // one launch: quantize the activation into bf16 codes and widen the weight
         ProfScope ps(kProfQuantize, 1, s);
         if (mode == CK_TENSORWISE)
@@ -372,7 +393,7 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
     p.y = y;
     p.residual = residual;
     p.out_dtype = out_dtype;
-    p.tail = ws.tail;
+    p.tail = graph ? nullptr : ws.tail;  // no K-split tail under capture
     std::string why;
     {
         ProfScope ps(kProfGemm, 1, s);
@@ -555,7 +576,7 @@ static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, co
     p.residual = acc ? nullptr : residual;
     p.out_dtype = out_dtype;
     p.acc = acc;
-    p.tail = tail;
+    p.tail = stream_capturing(s) ? nullptr : tail;  // no K-split tail under capture
     std::string why;
     {
         ProfScope ps(kProfGemm, 1, s);
