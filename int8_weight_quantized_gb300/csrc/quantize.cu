@@ -964,10 +964,27 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
     cudaError_t e = device_error_ptr(&err);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(quant::tensorwise_prep_kernel, grid, 256, 0, s, static_cast<const uint4*>(x), nvec,
-                      static_cast<quant::EpochSlot*>(scratch), next_prep_epoch(), static_cast<__nv_bfloat16*>(q16),
-                      x_scale, reinterpret_cast<const uint4*>(w8), w_n >> 4, static_cast<uint4*>(w16),
-                      (uint64_t)2000000000ull, err);
+    // The blocks wait for each other's maxima, so all of them must be resident at once: the
+    // grid is at most what fits on the device, and the launch is cooperative, which the
+    // runtime starts only when every block can be placed (another stream's kernels may
+    // hold part of the GPU).  Programmatic serialization keeps the launch overlapping the
+    // previous kernel's tail.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, quant::tensorwise_prep_kernel, static_cast<const uint4*>(x), nvec,
+                              static_cast<quant::EpochSlot*>(scratch), next_prep_epoch(),
+                              static_cast<__nv_bfloat16*>(q16), x_scale, reinterpret_cast<const uint4*>(w8),
+                              w_n >> 4, static_cast<uint4*>(w16), (uint64_t)2000000000ull, err);
 }
 
 cudaError_t launch_rotate_bf16(const void* x, int64_t M, int64_t K, void* a16, const int8_t* w8, int64_t w_n,
