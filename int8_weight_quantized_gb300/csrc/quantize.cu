@@ -618,11 +618,16 @@ __device__ __forceinline__ void fence_acq_rel_gpu()
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
+// The first `staged` vectors a thread loads in step 1 are also kept in dynamic shared
+// memory (slot j of thread t at [j][t]: conflict-free, only the thread itself reads it
+// back), so step 4 reads them from there instead of from L2 / HBM.
+constexpr int kMaxStagedVectors = 13;  // 52 KiB per block: four blocks still fit an SM
 __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
     const uint4* __restrict__ x, int64_t nvec, EpochSlot* slots, unsigned long long epoch,
     __nv_bfloat16* __restrict__ q16, float* __restrict__ xs, const uint4* __restrict__ w8, int64_t w_n16,
-    uint4* __restrict__ w16, uint64_t timeout_ns, unsigned int* err)
+    uint4* __restrict__ w16, uint64_t timeout_ns, unsigned int* err, int staged)
 {
+    extern __shared__ uint4 x_stage[];
     griddep_wait();
     griddep_launch_dependents();
     __shared__ float red[8];
@@ -630,7 +635,9 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
     const int G = (int)gridDim.x;
     // 1. this block's maximum, published
     __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
-    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec; base += UNROLL * stride) {
+    int slot = 0;  // vectors this thread has loaded so far
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec;
+         base += UNROLL * stride, slot += UNROLL) {
         uint4 v[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
@@ -638,8 +645,11 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
             v[u] = i < nvec ? ld_stream(x + i) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u)
+        for (int u = 0; u < UNROLL; ++u) {
             m2 = absmax8(m2, v[u]);
+            if (slot + u < staged)
+                x_stage[(slot + u) * 256 + threadIdx.x] = v[u];
+        }
     }
     float m = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
     if ((threadIdx.x & 31) == 0)
@@ -696,12 +706,17 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
         xs[0] = sc;
     // 4. quantize this block's slice
     const Quantizer qz(sc, false);
-    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec; base += UNROLL * stride) {
+    slot = 0;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec;
+         base += UNROLL * stride, slot += UNROLL) {
         uint4 v[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t i = base + u * stride;
-            v[u] = i < nvec ? ld_stream(x + i) : make_uint4(0, 0, 0, 0);
+            if (slot + u < staged)
+                v[u] = x_stage[(slot + u) * 256 + threadIdx.x];
+            else
+                v[u] = i < nvec ? ld_stream(x + i) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
@@ -918,7 +933,10 @@ int prep_capacity(const DeviceInfo& dev)
     int& c = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
     if (c == 0) {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant::tensorwise_prep_kernel, 256, 0) !=
+        const size_t smem = (size_t)quant::kMaxStagedVectors * 256 * sizeof(uint4);
+        if (cudaFuncSetAttribute(quant::tensorwise_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant::tensorwise_prep_kernel, 256, smem) !=
                 cudaSuccess ||
             per_sm <= 0)
             per_sm = 1;
@@ -960,6 +978,9 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
     const int64_t want = std::max<int64_t>(1, (nvec + 255) / 256);
     const int64_t cap = std::min<int64_t>(prep_capacity(dev), (int64_t)quant::kMaxSlotsPerThread * 256);
     const int grid = (int)std::min<int64_t>(std::min<int64_t>(want, cap), max_blocks);
+    // vectors per thread, and how many of them step 1 keeps on chip for step 4
+    const int64_t per_thread = (nvec + (int64_t)grid * 256 - 1) / ((int64_t)grid * 256);
+    const int staged = (int)std::min<int64_t>(per_thread, quant::kMaxStagedVectors);
     unsigned int* err = nullptr;
     cudaError_t e = device_error_ptr(&err);
     if (e != cudaSuccess)
@@ -972,7 +993,7 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = (size_t)staged * 256 * sizeof(uint4);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -984,7 +1005,7 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
     return cudaLaunchKernelEx(&cfg, quant::tensorwise_prep_kernel, static_cast<const uint4*>(x), nvec,
                               static_cast<quant::EpochSlot*>(scratch), next_prep_epoch(),
                               static_cast<__nv_bfloat16*>(q16), x_scale, reinterpret_cast<const uint4*>(w8),
-                              w_n >> 4, static_cast<uint4*>(w16), (uint64_t)2000000000ull, err);
+                              w_n >> 4, static_cast<uint4*>(w16), (uint64_t)2000000000ull, err, staged);
 }
 
 cudaError_t launch_rotate_bf16(const void* x, int64_t M, int64_t K, void* a16, const int8_t* w8, int64_t w_n,
