@@ -16,22 +16,26 @@
 // int32 sum is the true accumulator; it never leaves the SM.
 //
 // CTA pairs (the default when there are at least two 128-row tiles).  A 2-CTA cluster
-// computes a 256 x 256 tile with tcgen05 cta_group::2: each CTA holds 128 activation
-// rows and 128 of the 256 weight rows of every k-block in its own shared memory, the
-// leader CTA issues one 256x256x16 MMA that reads both CTAs' operands, and each CTA's
-// TMEM receives its own 128 output rows.  Per SM this halves the weight bytes that
-// shared memory must take in and hand to the tensor core, compared with one CTA per
-// 128 x 256 tile.  Problems with a single tile row run one CTA per 128 x 256 tile.
+// computes a 256 x bn tile (bn a multiple of 32 up to 256, chosen per launch) with
+// tcgen05 cta_group::2: each CTA holds 128 activation rows and bn/2 of the weight rows of
+// every k-block in its own shared memory, the leader CTA issues 256 x bn x 16 MMAs that
+// read both CTAs' operands, and each CTA's TMEM receives its own 128 output rows.  Per SM
+// this halves the weight bytes that shared memory must take in and hand to the tensor
+// core, compared with one CTA per 128 x bn tile.  Problems with a single tile row (and
+// one-wave problems the planner prices cheaper so) run one CTA per 128 x bn tile.
 //
-// Roles (one CTA per SM, 10 warps):
-//   warp 0     TMA producer: this CTA's A [128 x 64] and B [128 x 64] (pair) or B [256 x 64]
-//              (single) bf16 boxes per k-block into a ring of 128B-swizzled stages; in a
-//              pair, completion is counted on the leader's barrier;
-//   warp 1     allocates 512 TMEM columns (two fp32 accumulators of 256 columns) and, in
-//              the leader (or single CTA), issues the MMAs from one thread;
-//   warps 2-9  epilogue: warp w reads TMEM lanes 32*(w%4).. and one 128-column half;
-//              drains each chunk into its running sums, then dequantizes, converts to
-//              bf16, stages 32x32 boxes in shared memory and stores them with TMA.
+// Roles (one CTA per SM, 12 warps):
+//   warp 0      TMA producer: per k-block this CTA's A rows and B rows as 64-deep bf16
+//               boxes into a ring of 128B-swizzled stages -- CTA pairs stage 128-deep
+//               k-blocks (two boxes per operand, three stages), single CTAs 64-deep ones
+//               (four stages); in a pair, completion is counted on the leader's barrier;
+//   warp 1      allocates 512 TMEM columns (two fp32 accumulators of 256 columns) and, in
+//               the leader (or single CTA), issues the MMAs from one thread;
+//   warps 2-3   idle (they complete warpgroup 0 for the register re-balancing);
+//   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4).. and one 128-column half;
+//               drains each chunk into its running sums, then dequantizes, converts to
+//               the output type, stages 32-row boxes in shared memory and stores them
+//               with TMA.
 // The two accumulators ping-pong, so the MMA of the next chunk (or tile) overlaps the
 // drain and the store of the previous one.  Tiles are visited in a grouped order
 // (group_m unit rows share a sweep over N) so concurrently resident CTAs reuse operands
