@@ -78,3 +78,27 @@ def test_split_gemm_graph_replays_exact(monkeypatch):
         torch.cuda.synchronize()
         assert np.array_equal(acc.cpu().numpy(), refs[i])
     assert ck.ck_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("mode", [ck.TENSORWISE, ck.PER_ROW, ck.CONVROT])
+def test_w8a16_graph_replays_match_eager(mode):
+    """The 16-bit-activation layer (widening or rotation launch + GEMM) under capture."""
+    M, N, K = 384, 512, 1024
+    x0, x1, w, ws, b = _inputs(M, N, K, mode, 60 + mode)
+    ref0 = bits(ck.ck_w8a16_linear(x0, w, ws, b, mode=mode))
+    ref1 = bits(ck.ck_w8a16_linear(x1, w, ws, b, mode=mode))
+    x = x0.clone()
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    work = ck.workspace(max(16, ck.load_library().ck_w8a16_linear_workspace_size(M, N, K, mode)))
+    ck.ck_w8a16_linear(x, w, ws, b, mode=mode, y=y, ws=work)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ck.ck_w8a16_linear(x, w, ws, b, mode=mode, y=y, ws=work)
+    for src, ref in ((x1, ref1), (x0, ref0), (x1, ref1)):
+        x.copy_(src)
+        y.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(y), ref)
+    assert ck.ck_device_error(clear=True) == 0
