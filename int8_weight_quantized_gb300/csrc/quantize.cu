@@ -599,7 +599,7 @@ struct alignas(16) EpochSlot {
     float value;
     float pad;
 };
-constexpr int kMaxSlotsPerThread = 4;  // slots one of the 256 threads watches
+constexpr int kMaxSlotsPerThread = 4;  // slots one thread of the block watches
 
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p)
 {
@@ -621,8 +621,10 @@ __device__ __forceinline__ void fence_acq_rel_gpu()
 // The first `staged` vectors a thread loads in step 1 are also kept in dynamic shared
 // memory (slot j of thread t at [j][t]: conflict-free, only the thread itself reads it
 // back), so step 4 reads them from there instead of from L2 / HBM.
-constexpr int kMaxStagedVectors = 13;  // 52 KiB per block: four blocks still fit an SM
-__global__ void __launch_bounds__(256) tensorwise_prep_kernel(
+constexpr int kMaxStagedVectors = 13;  // 13 vectors per thread: 208 KiB of the SM
+constexpr int kPrepThreads = 256;      // threads per block
+template <int TPB>
+__global__ void __launch_bounds__(TPB) tensorwise_prep_kernel(
     const uint4* __restrict__ x, int64_t nvec, EpochSlot* slots, unsigned long long epoch,
     __nv_bfloat16* __restrict__ q16, float* __restrict__ xs, const uint4* __restrict__ w8, int64_t w_n16,
     uint4* __restrict__ w16, uint64_t timeout_ns, unsigned int* err, int staged)
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
     extern __shared__ uint4 x_stage[];
     griddep_wait();
     griddep_launch_dependents();
-    __shared__ float red[8];
+    __shared__ float red[TPB / 32];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int G = (int)gridDim.x;
     // 1. this block's maximum, published
@@ -648,7 +650,7 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
         for (int u = 0; u < UNROLL; ++u) {
             m2 = absmax8(m2, v[u]);
             if (slot + u < staged)
-                x_stage[(slot + u) * 256 + threadIdx.x] = v[u];
+                x_stage[(slot + u) * TPB + threadIdx.x] = v[u];
         }
     }
     float m = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
@@ -668,13 +670,13 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
     uint32_t seen = 0;
 #pragma unroll
     for (int j = 0; j < kMaxSlotsPerThread; ++j)
-        if ((int)threadIdx.x + 256 * j >= G)
+        if ((int)threadIdx.x + TPB * j >= G)
             seen |= 1u << j;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t round = 1;; ++round) {
 #pragma unroll
         for (int j = 0; j < kMaxSlotsPerThread; ++j)
-            if (!(seen & (1u << j)) && ld_relaxed_u64(&slots[threadIdx.x + 256 * j].epoch) == epoch)
+            if (!(seen & (1u << j)) && ld_relaxed_u64(&slots[threadIdx.x + TPB * j].epoch) == epoch)
                 seen |= 1u << j;
         int give_up = 0;
         if ((round & 15u) == 0 && threadIdx.x == 0 && globaltimer_ns() - t0 > timeout_ns)
@@ -691,8 +693,8 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
     m = 0.0f;
 #pragma unroll
     for (int j = 0; j < kMaxSlotsPerThread; ++j)
-        if ((int)threadIdx.x + 256 * j < G)
-            m = fmaxf(m, __ldcg(&slots[threadIdx.x + 256 * j].value));
+        if ((int)threadIdx.x + TPB * j < G)
+            m = fmaxf(m, __ldcg(&slots[threadIdx.x + TPB * j].value));
     m = warp_max(m);
     __syncthreads();  // every warp is done with red[] from step 1
     if ((threadIdx.x & 31) == 0)
@@ -714,7 +716,7 @@ __global__ void __launch_bounds__(256) tensorwise_prep_kernel(
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t i = base + u * stride;
             if (slot + u < staged)
-                v[u] = x_stage[(slot + u) * 256 + threadIdx.x];
+                v[u] = x_stage[(slot + u) * TPB + threadIdx.x];
             else
                 v[u] = i < nvec ? ld_stream(x + i) : make_uint4(0, 0, 0, 0);
         }
@@ -943,10 +945,11 @@ int prep_capacity(const DeviceInfo& dev)
     int& c = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
     if (c == 0) {
         int per_sm = 0;
-        const size_t smem = (size_t)quant::kMaxStagedVectors * 256 * sizeof(uint4);
-        if (cudaFuncSetAttribute(quant::tensorwise_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        constexpr int TPB = quant::kPrepThreads;
+        const size_t smem = (size_t)quant::kMaxStagedVectors * TPB * sizeof(uint4);
+        if (cudaFuncSetAttribute(quant::tensorwise_prep_kernel<TPB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant::tensorwise_prep_kernel, 256, smem) !=
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant::tensorwise_prep_kernel<TPB>, TPB, smem) !=
                 cudaSuccess ||
             per_sm <= 0)
             per_sm = 1;
@@ -985,11 +988,12 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
                                    cudaStream_t s)
 {
     const int64_t nvec = (M * K) >> 3;
-    const int64_t want = std::max<int64_t>(1, (nvec + 255) / 256);
-    const int64_t cap = std::min<int64_t>(prep_capacity(dev), (int64_t)quant::kMaxSlotsPerThread * 256);
+    constexpr int TPB = quant::kPrepThreads;
+    const int64_t want = std::max<int64_t>(1, (nvec + TPB - 1) / TPB);
+    const int64_t cap = std::min<int64_t>(prep_capacity(dev), (int64_t)quant::kMaxSlotsPerThread * TPB);
     const int grid = (int)std::min<int64_t>(std::min<int64_t>(want, cap), max_blocks);
     // vectors per thread, and how many of them step 1 keeps on chip for step 4
-    const int64_t per_thread = (nvec + (int64_t)grid * 256 - 1) / ((int64_t)grid * 256);
+    const int64_t per_thread = (nvec + (int64_t)grid * TPB - 1) / ((int64_t)grid * TPB);
     const int staged = (int)std::min<int64_t>(per_thread, quant::kMaxStagedVectors);
     unsigned int* err = nullptr;
     cudaError_t e = device_error_ptr(&err);
@@ -1002,8 +1006,8 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
     // previous kernel's tail.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = (size_t)staged * 256 * sizeof(uint4);
+    cfg.blockDim = dim3(TPB);
+    cfg.dynamicSmemBytes = (size_t)staged * TPB * sizeof(uint4);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -1012,7 +1016,7 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, quant::tensorwise_prep_kernel, static_cast<const uint4*>(x), nvec,
+    return cudaLaunchKernelEx(&cfg, quant::tensorwise_prep_kernel<TPB>, static_cast<const uint4*>(x), nvec,
                               static_cast<quant::EpochSlot*>(scratch), next_prep_epoch(),
                               static_cast<__nv_bfloat16*>(q16), x_scale, reinterpret_cast<const uint4*>(w8),
                               w_n >> 4, static_cast<uint4*>(w16), (uint64_t)2000000000ull, err, staged);
