@@ -7,7 +7,6 @@
 #include <string>
 #include <utility>
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace ck {
@@ -93,10 +92,6 @@ struct GemmPlan {
 };
 cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, bool mixed, const DeviceInfo& dev, GemmPlan* plan);
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s, std::string* why);
-// 2-D row-major tensor map of `rows` x `cols` elements (row pitch `pitch_bytes`), box
-// `box_rows` x `box_cols`; false (with a message in *why) when the driver rejects it.
-bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
-                 uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz, std::string* why);
 cudaError_t launch_quantize_rows(const void* x, int64_t M, int64_t K, bool rotate, int8_t* q8, void* q16,
                                  float* x_scale, const DeviceInfo& dev, cudaStream_t s);
 // Tensorwise quantize in two launches: per-block maxima into `partials`

@@ -702,8 +702,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 2-D row-major tensor of `rows` x `cols` elements with a row pitch of `pitch_bytes`.
-bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+// 2-D row-major tensor of `rows` x `cols` elements with a row pitch of `pitch_bytes`;
+// false (with a message in *why) when the driver rejects it.
+static bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
                  uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz, std::string* why)
 {
     auto fn = encode_fn();
