@@ -5,10 +5,13 @@ One step = one full pass of the layer's hot path, ck_int8_linear: the preparatio
 (activation quantize into bf16 codes, plus the int8 -> bf16 weight widening) and the
 tensor-core GEMM with the fused dequant/bias/bf16 epilogue, over one batch of seeded
 synthetic inputs that are already resident in device memory.  Metric: 2*M*N*K / step
-time, in TOPS.
+time, in TOPS.  The default workload is the largest per-row shape of the sweep,
+80666 x 28672 x 5376 (PR #142, "Numbers from the sweep").
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME]
+
+Without --steps the timed region runs as many steps as fill about 8 seconds (at least 20).
 
 Under torchrun (N > 1) every rank runs its own copy of the workload on its own GPU
 (independent problems, weak scaling, no collective on the data path); the step time is
@@ -40,7 +43,8 @@ METRIC = "INT8 linear TOPS (2MNK/s, fused dequant) and % of GB300 dense INT8 pea
 METRICS = {"int8": METRIC, "w8a16": "W8A16 linear TOPS (2MNK/s, bf16 activations x int8 weight codes)"}
 UNIT = "TOPS"
 WORKLOADS = {spec[0]: spec for spec in synthetic.ALL_WORKLOADS}
-DEFAULT_WORKLOAD = synthetic.TENSORWISE_4096[0]
+DEFAULT_WORKLOAD = synthetic.SWEEP[-1][0]  # per_row_80666x28672x5376
+TIMED_SECONDS = 8.0  # target length of the timed region when --steps is not given
 FLUSH_BYTES = 512 << 20  # > 129 MB of L2: written between steps (outside the timed events)
 CLEAN_BYTES = 256 << 20  # then read, so the step does not start by writing back the flush's dirty lines
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
@@ -234,15 +238,16 @@ def run_reference(args, spec):
     probe = min(M, max(4, oracle.num_threads()))
     t_probe = oracle_step_rows(case, probe, args.path)
     per_row = t_probe / probe
-    rows = int(max(1, min(M, budget / (args.steps + args.warmup) / per_row)))
+    steps = args.steps if args.steps is not None else 20
+    rows = int(max(1, min(M, budget / (steps + args.warmup) / per_row)))
     for _ in range(args.warmup):
         oracle_step_rows(case, rows, args.path)
-    times = [oracle_step_rows(case, rows, args.path) for _ in range(args.steps)]
+    times = [oracle_step_rows(case, rows, args.path) for _ in range(steps)]
     step_s = sum(times) / len(times)
     value = 2.0 * rows * N * K / step_s / 1e12
     sample = "first %d of %d rows x all %d columns, K=%d, per step" % (rows, M, N, K)
     line = {"impl": "reference", "metric": METRICS[args.path], "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8" if args.path == "int8" else "bf16",
             "data": "synthetic",
             "config": workload_config(spec, "n/a (host)"),
@@ -302,11 +307,22 @@ def run_ours(args, spec):
     torch.cuda.synchronize()
     if ck.ck_device_error(clear=True) != 0:
         raise SystemExit("a kernel reported a wait timeout during warm-up")
+    steps = args.steps
+    if steps is None:
+        # size the timed region from one more (untimed) step: about TIMED_SECONDS of steps
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush_l2(0)
+        e0.record()
+        step()
+        e1.record()
+        torch.cuda.synchronize()
+        one = reduce_max(e0.elapsed_time(e1), dev)
+        steps = int(min(4000, max(20, TIMED_SECONDS * 1e3 / max(one, 1e-3))))
 
-    # ---- timed region: K steps, device-resident inputs, L2 flushed between steps.  The
-    # library only counts its launches here (no events between its kernels, so their
+    # ---- timed region: `steps` steps, device-resident inputs, L2 flushed between steps.
+    # The library only counts its launches here (no events between its kernels, so their
     # programmatic launch overlap is what gets timed).
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -324,14 +340,14 @@ def run_ours(args, spec):
     barrier()
     counts = ck.ck_profile_end()
     clocks = sampler.stop()
-    step_ms_local = sum(a.elapsed_time(b_) for a, b_ in evs) / args.steps
+    step_ms_local = sum(a.elapsed_time(b_) for a, b_ in evs) / steps
     step_ms = reduce_max(step_ms_local, dev)
     value = world * ops / (step_ms * 1e-3) / 1e12
     if ck.ck_device_error(clear=True) != 0:
         raise SystemExit("a kernel reported a wait timeout in the timed region")
 
     # ---- per-kernel durations: the same loop with CUDA events around each library launch
-    kt_steps = min(args.steps, 1000)
+    kt_steps = min(steps, 1000)
     barrier()
     torch.cuda.synchronize()
     ck.ck_profile_begin(with_events=True)
@@ -349,31 +365,44 @@ def run_ours(args, spec):
     gemm_avg_ms = reduce_max(g_ms / max(g_n, 1), dev)
     achieved = ops / (gemm_avg_ms * 1e-3) / 1e12
     traffic = None if w8a16 else profiled_traffic(name)
-    # preparation, algorithmic bytes: read x (bf16) once, write its bf16 codes, read the
-    # int8 weight, write its bf16 codes, plus the scales
-    # (the 16-bit path: the weight widening, plus read x / write bf16(x @ H) for ConvRot)
+    # The preparation launch.  Algorithmic bytes (the activation quantize alone): read x
+    # (bf16) and write int8 codes, 3 B per element, plus 4 B per row scale; tensorwise
+    # reads x twice (5 B per element).  Moved bytes (what the launch really does, the
+    # bf16-operand engine's overhead included): x read, its codes written as bf16, the int8
+    # weight read and written as bf16 codes.  The 16-bit path: the weight widening, plus
+    # read x / write bf16(x @ H) for ConvRot.
     if w8a16:
-        prep_bytes = N * K + 2 * N * K + (4 * M * K if mode == synthetic.CONVROT else 0)
+        prep_alg = 4 * M * K if mode == synthetic.CONVROT else 0
+        prep_moved = N * K + 2 * N * K + prep_alg
     else:
-        prep_bytes = 2 * M * K + 2 * M * K + N * K + 2 * N * K + 4 * M
+        prep_alg = (5 * M * K + 4) if mode == synthetic.TENSORWISE else (3 * M * K + 4 * M)
+        prep_moved = 2 * M * K + 2 * M * K + N * K + 2 * N * K + (4 if mode == synthetic.TENSORWISE else 4 * M)
     p_step = max(p_ms, 1e-9) / kt_steps
     roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
                 "frac": achieved / bf16_peak, "traffic": traffic,
                 "kernel": ("gemm_kernel<mixed> (tcgen05 kind::f16, bf16 activations x int8 codes, fp32 sum)" if w8a16
                            else "gemm_kernel (tcgen05 kind::f16 on int8 codes, exact int32, fused dequant)"),
-                "peak_source": "%s bf16 dense (burst); sustained %.1f" % (provenance, bf16_sust),
-                "avg_launch_ms": gemm_avg_ms, "timed_launches": g_n}
+                "peak_source": "%s bf16 dense, burst (cuBLAS); the engine this kernel runs on" % provenance,
+                "peak_sustained": bf16_sust, "frac_sustained": achieved / bf16_sust,
+                "avg_launch_ms": gemm_avg_ms, "timed_launches": g_n,
+                "algorithmic_flops_per_launch": ops}
     kernels = {
         "gemm": {"ms_per_step": g_ms / kt_steps, "launches": g_n},
-        "prep": {"ms_per_step": p_step, "launches": p_n, "bytes": prep_bytes,
-                 "GB/s": prep_bytes / (p_step * 1e-3) / 1e9,
-                 "frac_hbm": prep_bytes / (p_step * 1e-3) / 1e9 / hbm_peak},
+        "prep": {"ms_per_step": p_step, "launches": p_n,
+                 "bytes_algorithmic": prep_alg, "bytes_moved": prep_moved,
+                 "GB/s_algorithmic": prep_alg / (p_step * 1e-3) / 1e9,
+                 "GB/s_moved": prep_moved / (p_step * 1e-3) / 1e9,
+                 "frac_hbm_algorithmic": prep_alg / (p_step * 1e-3) / 1e9 / hbm_peak,
+                 "frac_hbm_moved": prep_moved / (p_step * 1e-3) / 1e9 / hbm_peak},
     }
+    if not w8a16:
+        kernels["quantize_int8"] = time_quantize_int8(ck, x, mode, flush_l2, min(kt_steps, 200), hbm_peak, dev)
 
     # ---- end to end through the same call, from and to pinned host memory
-    e2e_steps = max(20, min(args.steps, 500))
-    x_host = case.x.pin_memory()
-    y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(20, min(steps, 500))
+    x_host = torch.empty((M, K), dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(case.x)
+    y_host = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
     e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
     barrier()
     torch.cuda.synchronize()
@@ -389,10 +418,11 @@ def run_ours(args, spec):
     e2e = {"value": world * ops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,
            "d2h_bytes_per_step": y_host.numel() * 2, "ms_per_step": e2e_ms}
 
-    line = {"metric": METRICS[args.path], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+    line = {"metric": METRICS[args.path], "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int8" if not w8a16 else "bf16", "data": "synthetic",
-            "config": workload_config(spec, "flushed between steps (%d MiB write, then %d MiB read)" % (FLUSH_BYTES >> 20, CLEAN_BYTES >> 20)),
+            "config": workload_config(spec, "flushed between steps (%d MiB write, then %d MiB read); inputs %s L2" % (
+                FLUSH_BYTES >> 20, CLEAN_BYTES >> 20, "larger than" if M * K * 2 > (129 << 20) else "smaller than")),
             "roofline": roofline, "kernels": kernels, "e2e": e2e, "clocks": clocks,
             "gpu_launches": int(sum(n for _, n in counts.values())), "timed_wall_s": wall}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -404,10 +434,45 @@ def run_ours(args, spec):
     return 0
 
 
+def time_quantize_int8(ck, x, mode, flush_l2, n, hbm_peak, dev):
+    """The stand-alone activation quantize (ck_quantize_int8_rowwise, rotated for ConvRot,
+    or ck_quantize_int8_tensorwise): bf16 x in, int8 codes and fp32 scales out, each launch
+    bracketed by CUDA events on the launching stream, L2 flushed before it."""
+    M, K = x.shape
+    tw = mode == synthetic.TENSORWISE
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    xs = torch.empty((1 if tw else M,), dtype=torch.float32, device=dev)
+
+    def run():
+        if tw:
+            ck.ck_quantize_int8_tensorwise(x, q=q, x_scale=xs)
+        else:
+            ck.ck_quantize_int8_rowwise(x, rotate=(mode == synthetic.CONVROT), q=q, x_scale=xs)
+
+    for i in range(3):
+        flush_l2(i)
+        run()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for i, (e0, e1) in enumerate(evs):
+        flush_l2(i)
+        e0.record()
+        run()
+        e1.record()
+    torch.cuda.synchronize()
+    ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs) / n, dev)
+    nbytes = (5 * M * K + 4) if tw else (3 * M * K + 4 * M)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"entry": "ck_quantize_int8_tensorwise" if tw else "ck_quantize_int8_rowwise",
+            "rotate": mode == synthetic.CONVROT, "ms": ms, "launches": n, "bytes_algorithmic": nbytes,
+            "GB/s": gbs, "frac_hbm": gbs / hbm_peak, "peak_hbm_gbs": hbm_peak}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: as many as fill about %g s, at least 20)" % TIMED_SECONDS)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)

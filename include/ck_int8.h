@@ -39,7 +39,8 @@
  *     (after the shape checks); the buffers sized by M may then be NULL.
  *   - Device: compute capability 10.3 (GB300) only, else CK_ERR_UNSUPPORTED_DEVICE.
  *     There is no fallback path of any kind.
- *   - CUDA graphs: every entry point may be captured (cudaStreamBeginCapture) and the
+ *   - CUDA graphs: every entry point except ck_quantize_int8_tensorwise_noalloc (whose
+ *     capture is not covered here) may be captured (cudaStreamBeginCapture) and the
  *     graph replayed with new data in the same buffers; the results equal uncaptured
  *     calls.  Make one uncaptured call per device first (it sets kernel attributes and
  *     looks up the library's device symbols).  Under capture, ck_int8_linear in
@@ -47,6 +48,10 @@
  *     (the single launch exchanges block maxima under a per-call tag, which a replay would
  *     repeat), and no GEMM splits its last wave along K (the split's arrival counters are
  *     tagged the same way): same results, a few microseconds slower per call.
+ *   - Bounded waits: kernels whose threads wait on each other give up after 2 s instead
+ *     of hanging, record a bit in a device error word and exit normally; the entry point
+ *     that enqueued them has long returned CK_OK by then.  ck_device_error() reads that
+ *     word: a caller that must know a result is sound checks it after synchronizing.
  */
 #ifndef CK_INT8_H
 #define CK_INT8_H
@@ -102,17 +107,23 @@ size_t ck_quantize_tensorwise_workspace_size(void);
 int ck_quantize_int8_tensorwise(const void *x, int64_t M, int64_t K, int8_t *q, float *x_scale,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
-/* Tensorwise quantize for callers that cannot allocate device memory (code running
- * under CUDA graph capture, fixed-budget real-time loops, hosts whose own allocator must
- * own every byte).  No counterpart on the pages: it computes exactly what
- * ck_quantize_int8_tensorwise computes, but keeps its partial maxima in a 16 KiB array
- * built into the library (present on every GPU that loads it, until exit) instead of a
- * caller workspace, and calls no allocation routine.
+/* Tensorwise quantize for callers that cannot allocate device memory.  The pages have no
+ * counterpart of this entry point.  It serves code that may not touch an allocator while
+ * it runs: real-time loops that reserve their whole memory budget up front (an
+ * allocation can block, or fail on a fragmented heap, at a moment they cannot afford),
+ * hosts whose own memory manager must account for every byte on the device, and plugins
+ * inside such hosts, which see only the buffers they are handed.  It computes exactly
+ * what ck_quantize_int8_tensorwise computes, but keeps its partial maxima in a 16 KiB
+ * array built into the library (present on every GPU that loads it, until the process
+ * exits) instead of a caller workspace, and calls no allocation routine.
  *   x, q, x_scale: as for ck_quantize_int8_tensorwise (caller-owned device buffers).
- *   Limit: M*K <= 134,217,728 values, else CK_ERR_INVALID_ARG.
- *   The first call on a device looks up the array's address there; make it before any
- *   stream capture.  All calls share the array: calls that overlap on the GPU (other
- *   streams or threads) race; serialize them. */
+ *   Limit: M*K <= 134,217,728 values, else CK_ERR_INVALID_ARG (nothing enqueued).
+ *   The first call in a CUDA context looks up the array's device address there and keeps
+ *   it; make that first call before any stream capture begins.  After a device reset the
+ *   next call looks it up again.  All calls share the array, which keeps the last call's
+ *   contents (nothing in it has to start at zero: a call reads only slots it wrote
+ *   itself), so calls that overlap on the GPU (other streams or threads) race and may
+ *   return a wrong scale: serialize them. */
 int ck_quantize_int8_tensorwise_noalloc(const void *x, int64_t M, int64_t K, int8_t *q, float *x_scale,
                                         void *stream);
 
@@ -120,6 +131,20 @@ int ck_quantize_int8_tensorwise_noalloc(const void *x, int64_t M, int64_t K, int
  * workspace holds the quantized activation and the weight as bf16 integers (the
  * tensor-core operand format), the activation scales and the tensorwise partial maxima. */
 size_t ck_int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
+
+/* Where ck_int8_linear leaves, in the caller's workspace, the activation quantize of its
+ * last call (issue #278, section "2. quantize_int8_rowwise raises instead of falling
+ * back": the codes q and the scales; issue #280, "Exactness": tensor-wide scales):
+ *   *codes_offset:   byte offset of q as bf16 integers [M,K] row-major (every value an
+ *                    integer in [-127, 127], exact in bf16; a zero may carry either sign);
+ *   *x_scale_offset: byte offset of x_scale fp32 [M] (CK_PER_ROW, CK_CONVROT) or [1]
+ *                    (CK_TENSORWISE).
+ * The layout depends only on (M, N, K, mode), so a test can read what the layer's own
+ * preparation kernel computed and compare it with a reference bit for bit.  Host only:
+ * nothing is enqueued.  CK_ERR_INVALID_ARG for a bad mode, negative sizes or NULL
+ * outputs. */
+int ck_int8_linear_workspace_views(int64_t M, int64_t N, int64_t K, int mode, size_t *codes_offset,
+                                   size_t *x_scale_offset);
 
 /* The INT8 linear layer (issue #136 repro API int8_linear(x, w, ws, out_dtype) with
  * the optional bias of issue #280):
@@ -136,7 +161,11 @@ size_t ck_int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
  *            ck_dtype_t.
  *   workspace/workspace_bytes: device scratch of ck_int8_linear_workspace_size() bytes.
  * No int32 intermediate is ever written to device memory.  An out_dtype outside
- * ck_dtype_t gives CK_ERR_INVALID_ARG. */
+ * ck_dtype_t gives CK_ERR_INVALID_ARG.
+ * In CK_TENSORWISE mode the preparation kernel's blocks exchange their maxima and wait
+ * for each other (bounded, 2 s).  A block that gives up makes x_scale NaN, so every
+ * element of y is NaN rather than plausible, and sets a bit in the device error word:
+ * ck_device_error() is how a caller learns of it. */
 int ck_int8_linear(const void *x, const int8_t *w, const float *w_scale, const void *bias, const void *residual,
                    void *y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype, void *workspace,
                    size_t workspace_bytes, void *stream);

@@ -49,6 +49,7 @@ def load_library(path=None):
         "ck_quantize_int8_tensorwise": ([P, I64, I64, P, P, P, SZ, P], I),
         "ck_quantize_int8_tensorwise_noalloc": ([P, I64, I64, P, P, P], I),
         "ck_int8_linear_workspace_size": ([I64, I64, I64, I], SZ),
+        "ck_int8_linear_workspace_views": ([I64, I64, I64, I, ctypes.POINTER(SZ), ctypes.POINTER(SZ)], I),
         "ck_int8_linear": ([P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_convrot_prepare_weight": ([P, I64, I64, P, P, P], I),
         "ck_int8_gemm_workspace_size": ([I64, I64, I64], SZ),
@@ -154,6 +155,25 @@ def ck_quantize_int8_tensorwise_noalloc(x, q, x_scale, stream=None):
 
 def ck_int8_linear_workspace_size(M, N, K, mode):
     return load_library().ck_int8_linear_workspace_size(M, N, K, int(mode))
+
+
+def ck_int8_linear_workspace_views(M, N, K, mode):
+    """(codes_offset, x_scale_offset): byte offsets in ck_int8_linear's workspace of the
+    activation codes (bf16 integers [M,K]) and x_scale (fp32 [M], or [1] in tensorwise
+    mode) left by the last call."""
+    codes, xs = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load_library().ck_int8_linear_workspace_views(M, N, K, int(mode), ctypes.byref(codes), ctypes.byref(xs)))
+    return codes.value, xs.value
+
+
+def linear_workspace_codes(ws, M, N, K, mode):
+    """Views into a ck_int8_linear workspace (a uint8 device tensor): the activation codes
+    as bf16 [M,K] and x_scale fp32 [M] or [1], as the layer's last call left them."""
+    co, xo = ck_int8_linear_workspace_views(M, N, K, mode)
+    codes = ws[co:co + 2 * M * K].view(torch.bfloat16).view(M, K)
+    n = 1 if mode == TENSORWISE else M
+    x_scale = ws[xo:xo + 4 * n].view(torch.float32)
+    return codes, x_scale
 
 
 def _out_code(out_dtype):

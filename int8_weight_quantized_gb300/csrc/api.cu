@@ -12,6 +12,7 @@
 #include <tuple>
 #include <vector>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ck_int8.h"
@@ -209,20 +210,63 @@ cudaError_t current_device(DeviceInfo* info)
     return cudaSuccess;
 }
 
-void log_shape(const char* what, int64_t M, int64_t N, int64_t K, int mode, const char* engine)
+cudaError_t current_context_id(unsigned long long* id)
+{
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+    });
+    if (get_current == nullptr || get_id == nullptr)
+        return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS)
+        return cudaErrorDeviceUninitialized;
+    if (ctx == nullptr) {
+        // nothing current yet: the runtime would create the device's primary context on
+        // its first real call; do that now so the id is the one later calls will see
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaSetDevice(dev);
+        if (e != cudaSuccess)
+            return e;
+        if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+            return cudaErrorDeviceUninitialized;
+    }
+    return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+bool log_enabled()
 {
     static const bool on = [] {
         const char* v = std::getenv("CK_LOG");
         return v && v[0] == '1';
     }();
-    if (!on)
+    return on;
+}
+
+void log_shape(const char* what, int64_t M, int64_t N, int64_t K, int mode, const std::string& engine)
+{
+    if (!log_enabled())
         return;
     static std::mutex mu;
     static std::set<std::tuple<std::string, int64_t, int64_t, int64_t, int>> seen;
     std::lock_guard<std::mutex> lock(mu);
     if (seen.insert(std::make_tuple(std::string(what), M, N, K, mode)).second)
         fprintf(stderr, "[ck] %s M=%lld N=%lld K=%lld mode=%d engine=%s\n", what, (long long)M, (long long)N,
-                (long long)K, mode, engine);
+                (long long)K, mode, engine.c_str());
 }
 
 }  // namespace ck
@@ -256,7 +300,7 @@ int ck_quantize_int8_rowwise(const void* x, int64_t M, int64_t K, int rotate, in
     int st = check_device(&dev);
     if (st != CK_OK)
         return st;
-    log_shape("quantize_rowwise", M, 0, K, rotate ? CK_CONVROT : CK_PER_ROW, "rows-warp");
+    log_shape("quantize_rowwise", M, 0, K, rotate ? CK_CONVROT : CK_PER_ROW, "rows (32-256 threads per row)");
     cudaError_t e;
     {
         ProfScope ps(kProfQuantize, 1, static_cast<cudaStream_t>(stream));
@@ -290,7 +334,7 @@ int ck_quantize_int8_tensorwise(const void* x, int64_t M, int64_t K, int8_t* q, 
     int st = check_device(&dev);
     if (st != CK_OK)
         return st;
-    log_shape("quantize_tensorwise", M, 0, K, CK_TENSORWISE, "flat-two-pass");
+    log_shape("quantize_tensorwise", M, 0, K, CK_TENSORWISE, "block maxima, then quantize (2 launches)");
     cudaError_t e;
     {
         ProfScope ps(kProfQuantize, 2, static_cast<cudaStream_t>(stream));
@@ -305,6 +349,22 @@ size_t ck_int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int mode)
     if (M < 0 || N < 0 || K < 0)
         return 0;
     return linear_ws_bytes(M, N, K, mode, kMaxPartials);
+}
+
+int ck_int8_linear_workspace_views(int64_t M, int64_t N, int64_t K, int mode, size_t* codes_offset,
+                                   size_t* x_scale_offset)
+{
+    if (mode != CK_TENSORWISE && mode != CK_PER_ROW && mode != CK_CONVROT)
+        return fail(CK_ERR_INVALID_ARG, "mode must be 0 (tensorwise), 1 (per-row) or 2 (ConvRot), got %d", mode);
+    if (M < 0 || N < 0 || K < 0)
+        return fail(CK_ERR_INVALID_ARG, "M, N and K must be >= 0");
+    if (codes_offset == nullptr || x_scale_offset == nullptr)
+        return fail(CK_ERR_INVALID_ARG, "codes_offset and x_scale_offset must not be NULL");
+    uint8_t* const base = reinterpret_cast<uint8_t*>(kAlign);  // any aligned base: only differences are used
+    const LinearWorkspace w = carve_linear(base, M, N, K, mode);
+    *codes_offset = (size_t)(static_cast<uint8_t*>(w.a16) - base);
+    *x_scale_offset = (size_t)(reinterpret_cast<uint8_t*>(w.xs) - base);
+    return CK_OK;
 }
 
 // Whether work enqueued on `s` is being captured into a CUDA graph.  A captured launch
@@ -358,10 +418,14 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
         return st;
     if (M == 0)
         return CK_OK;
-    log_shape("int8_linear", M, N, K, mode, "prep(1 launch) + tcgen05 bf16-exact GEMM, 2-CTA 256x256 tiles");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     LinearWorkspace ws = carve_linear(workspace, M, N, K, mode);
     const bool graph = stream_capturing(s);
+    if (log_enabled())
+        log_shape("int8_linear", M, N, K, mode,
+                  std::string(mode == CK_TENSORWISE && graph ? "quantize (2 launches) + widening"
+                                                             : "preparation (1 launch)") +
+                      " + tcgen05 bf16-exact GEMM, " + describe_gemm_plan(M, N, K, false, !graph, dev));
     cudaError_t e;
     if (mode == CK_TENSORWISE && graph) {
         // captured: per-block maxima, a quantize pass that reduces them, the widening apart
@@ -447,7 +511,11 @@ int ck_w8a16_linear(const void* x, const int8_t* w, const float* w_scale, const 
     DeviceInfo dev;
     if ((st = check_device(&dev)) != CK_OK)
         return st;
-    log_shape("w8a16_linear", M, N, K, mode, "widen (+ rotate) + tcgen05 bf16 GEMM, fp32 sum over K");
+    if (log_enabled())
+        log_shape("w8a16_linear", M, N, K, mode,
+                  std::string(mode == CK_CONVROT ? "rotate + widen" : "widen") +
+                      " (1 launch) + tcgen05 bf16 GEMM with an fp32 sum over K, " +
+                      describe_gemm_plan(M, N, K, true, false, dev));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* p8 = static_cast<uint8_t*>(workspace);
     void* b16 = p8;
@@ -549,8 +617,11 @@ static int gemm_entry(const int8_t* q, const float* x_scale, const int8_t* w, co
         return st;
     if (M == 0)
         return CK_OK;
-    log_shape(name, M, N, K, scalar_scales ? CK_TENSORWISE : CK_PER_ROW, "widen(1 launch) + tcgen05 bf16-exact GEMM, 2-CTA 256x256 tiles");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (log_enabled())
+        log_shape(name, M, N, K, scalar_scales ? CK_TENSORWISE : CK_PER_ROW,
+                  "widen (1 launch) + tcgen05 bf16-exact GEMM, " +
+                      describe_gemm_plan(M, N, K, false, !stream_capturing(s), dev));
     uint8_t* p8 = static_cast<uint8_t*>(workspace);
     void* a16 = p8;
     void* b16 = p8 + align_up((size_t)M * K * 2);
@@ -703,27 +774,31 @@ int ck_selftest_wait_timeout(uint64_t timeout_ns, void* stream)
 // ---------------------------------------------------------------------------------
 // Tensorwise quantize without any allocation.
 //
-// Some callers cannot allocate device memory at all: code that runs while a CUDA graph
-// is being captured (cudaMalloc is not a capturable operation), real-time inference
-// loops that own a fixed memory budget and forbid allocator traffic, and hosts that
-// embed this library under another allocator which must see every byte.  They can
-// still pass their inputs and outputs, but not a workspace.  For them the partial
-// maxima of the tensorwise quantize live in a fixed array that is part of the loaded
-// module itself.
+// Some callers cannot allocate device memory at all.  A real-time inference loop may
+// reserve its whole memory budget before it starts and forbid allocator traffic while it
+// runs: an allocation can block, or fail on a fragmented heap, at a moment the loop
+// cannot afford.  A host that embeds this library under its own memory manager must
+// account for every byte on the device and hands out nothing per call, and a plugin
+// loaded into such a host sees only the buffers it is given.  These callers can pass
+// their inputs and outputs, but not a workspace.  For them the partial maxima of the
+// tensorwise quantize live in a fixed array that is part of the loaded module itself.
 //
-// Costs and limits, stated plainly:
+// Costs and limits:
 //   - the array holds kNoallocMaxPartials floats (16 KiB) on every GPU where this
 //     library's module is loaded, for the life of the process;
 //   - one partial maximum covers kNoallocValuesPerPartial input values, so M*K may be
 //     at most kNoallocMaxPartials * kNoallocValuesPerPartial = 134,217,728 values;
-//     larger tensors are rejected with CK_ERR_INVALID_ARG;
-//   - every call uses the same array.  Nothing in it needs to start at zero (each slot
-//     a call reads was written earlier by that same call), but two calls whose kernels
-//     overlap on the GPU -- different streams, or different host threads -- race on it
-//     and may return a wrong scale.  Serialize such calls on one stream;
-//   - the first call on a device looks up the array's device address on that device
-//     (cudaGetSymbolAddress, which also loads the module there).  Make that first call
-//     before any stream capture begins.
+//     larger tensors are rejected with CK_ERR_INVALID_ARG before anything is enqueued;
+//   - every call uses the same array and it keeps the last call's contents.  Nothing in
+//     it needs to start at zero: every slot a call reads was written earlier by that same
+//     call.  But two calls whose kernels overlap on the GPU -- different streams, or
+//     different host threads -- race on it and may return a wrong scale.  Serialize such
+//     calls on one stream;
+//   - the first call in a CUDA context looks up the array's device address there
+//     (cudaGetSymbolAddress, with that context's device current; this also loads the
+//     module on the device) and keeps it for later calls in the same context.  Make that
+//     first call before any stream capture begins.  A device reset creates a new context,
+//     whose first call looks the address up again.
 namespace ck {
 namespace {
 
@@ -733,24 +808,19 @@ constexpr int64_t kNoallocValuesPerPartial = kNoallocVectorsPerPartial * 8;
 
 static __device__ __align__(256) float g_noalloc_partials[kNoallocMaxPartials];
 
-// Device address of g_noalloc_partials on the current device, looked up once per device.
-// (In host code the array's name is only a host-side stand-in, never a device address.)
-int noalloc_scratch(const DeviceInfo& dev, float** out)
+// Device address of g_noalloc_partials in the current context.  In host code the
+// array's name is only a host-side stand-in, never a device address: a kernel given it
+// would fault, or silently use the wrong memory where the GPU can reach host memory.
+int noalloc_scratch(float** out)
 {
-    static std::mutex mu;
-    static float* addr[64] = {};
-    if (dev.device < 0 || dev.device >= 64)
-        return fail(CK_ERR_UNSUPPORTED_DEVICE, "device ordinal %d is out of range", dev.device);
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev.device] == nullptr) {
-        void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_partials);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "looking up the no-allocation scratch array");
-        addr[dev.device] = static_cast<float*>(p);
-    }
-    *out = addr[dev.device];
-    return CK_OK;
+    static ContextCache<float*> cache;
+    const cudaError_t e = cache.get(out, [](float** p) {
+        void* a = nullptr;
+        const cudaError_t r = cudaGetSymbolAddress(&a, g_noalloc_partials);
+        *p = static_cast<float*>(a);
+        return r;
+    });
+    return e == cudaSuccess ? CK_OK : cuda_fail(e, "looking up the no-allocation scratch array");
 }
 
 }  // namespace
@@ -779,7 +849,7 @@ extern "C" int ck_quantize_int8_tensorwise_noalloc(const void* x, int64_t M, int
     if (st != CK_OK)
         return st;
     float* partials = nullptr;
-    if ((st = noalloc_scratch(dev, &partials)) != CK_OK)
+    if ((st = noalloc_scratch(&partials)) != CK_OK)
         return st;
     const int64_t nvec = (M * K) >> 3;
     const int nparts = (int)((nvec + kNoallocVectorsPerPartial - 1) / kNoallocVectorsPerPartial);

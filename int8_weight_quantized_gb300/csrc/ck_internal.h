@@ -4,8 +4,10 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <string>
 #include <utility>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -59,6 +61,44 @@ struct DeviceInfo {
 
 // Query (once per device) and return the current device's properties.
 cudaError_t current_device(DeviceInfo* info);
+
+// Identifier of the CUDA context current on this host thread, unique for the life of
+// the process (the driver's context id).  With no context current yet, the current
+// device's primary context is made current first.
+cudaError_t current_context_id(unsigned long long* id);
+
+// A value that belongs to a CUDA context (a device address of one of the library's
+// variables, a kernel attribute set on it), made once per context by make(&value) while
+// that context is current.  A device reset creates a new context with a new id, so the
+// value is made again there instead of reusing what belonged to the destroyed one.
+template <typename T>
+class ContextCache {
+public:
+    template <typename Make>
+    cudaError_t get(T* out, Make make)
+    {
+        unsigned long long id = 0;
+        cudaError_t e = current_context_id(&id);
+        if (e != cudaSuccess)
+            return e;
+        std::lock_guard<std::mutex> lock(mu_);
+        for (const auto& kv : entries_)
+            if (kv.first == id) {
+                *out = kv.second;
+                return cudaSuccess;
+            }
+        T v{};
+        if ((e = make(&v)) != cudaSuccess)
+            return e;
+        entries_.emplace_back(id, v);
+        *out = v;
+        return cudaSuccess;
+    }
+
+private:
+    std::mutex mu_;
+    std::vector<std::pair<unsigned long long, T>> entries_;
+};
 
 // Kernel launchers.  Each returns cudaSuccess or the launch error; `why` gets a
 // description of a failure that is not a CUDA error.
@@ -134,7 +174,12 @@ cudaError_t launch_widen_int8(const int8_t* src, void* dst, int64_t n, const Dev
 cudaError_t read_device_error(unsigned int* value, bool clear);
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s);
 
-// Diagnostics: one line per unique problem shape when CK_LOG=1.
-void log_shape(const char* what, int64_t M, int64_t N, int64_t K, int mode, const char* engine);
+// Diagnostics: one line per unique problem shape when CK_LOG=1 (log_enabled()).
+bool log_enabled();
+void log_shape(const char* what, int64_t M, int64_t N, int64_t K, int mode, const std::string& engine);
+// "<bn>-wide tiles on CTA pairs / single CTAs, K split s ways in the last wave" for the
+// GEMM an M x N x K launch would run (for the CK_LOG lines).
+std::string describe_gemm_plan(int64_t M, int64_t N, int64_t K, bool mixed, bool split_allowed,
+                               const DeviceInfo& dev);
 
 }  // namespace ck

@@ -731,27 +731,27 @@ static bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ba
 template <bool RAW, bool PAIR, int OUT, bool MIXED, bool SPLIT, bool RES>
 static cudaError_t ensure_smem_attr(int device)
 {
-    static bool done[64] = {};
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
-    if (device >= 0 && device < 64 && done[device])
-        return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT, RES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemm::Mode<PAIR>::SMEM_BYTES);
-    if (e == cudaSuccess) {
-        // the warpgroups' register re-balancing must fit in what a block is launched
-        // with (registers are granted per warp in units of 8 per thread), else the
-        // epilogue's increase would wait forever: refuse to launch instead
-        cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT, RES>);
-        if (e == cudaSuccess &&
-            (uint64_t)((fa.numRegs + 7) / 8 * 8) * gemm::THREADS < (uint64_t)gemm::REGS_NEEDED_PER_BLOCK)
-            e = cudaErrorInvalidConfiguration;
-    }
-    if (e == cudaSuccess && device >= 0 && device < 64)
-        done[device] = true;
-    return e;
+    (void)device;
+    // a kernel attribute belongs to the context it was set in: set once per context
+    static ContextCache<int> cache;
+    int done = 0;
+    return cache.get(&done, [](int* d) {
+        cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT, RES>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)gemm::Mode<PAIR>::SMEM_BYTES);
+        if (e == cudaSuccess) {
+            // the warpgroups' register re-balancing must fit in what a block is launched
+            // with (registers are granted per warp in units of 8 per thread), else the
+            // epilogue's increase would wait forever: refuse to launch instead
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<RAW, PAIR, OUT, MIXED, SPLIT, RES>);
+            if (e == cudaSuccess &&
+                (uint64_t)((fa.numRegs + 7) / 8 * 8) * gemm::THREADS < (uint64_t)gemm::REGS_NEEDED_PER_BLOCK)
+                e = cudaErrorInvalidConfiguration;
+        }
+        *d = 1;
+        return e;
+    });
 }
 
 static cudaLaunchConfig_t make_config(bool pair, size_t smem, cudaStream_t s, cudaLaunchAttribute (&attr)[2])
@@ -965,6 +965,23 @@ cudaError_t plan_gemm(int64_t M, int64_t N, int64_t K, bool mixed, const DeviceI
     return cudaSuccess;
 }
 
+std::string describe_gemm_plan(int64_t M, int64_t N, int64_t K, bool mixed, bool split_allowed,
+                               const DeviceInfo& dev)
+{
+    GemmPlan plan;
+    if (plan_gemm(std::max<int64_t>(M, 1), N, K, mixed, dev, &plan) != cudaSuccess)
+        return "no GEMM plan (device query failed)";
+    char buf[192];
+    const int split = split_allowed ? plan.split : 1;
+    snprintf(buf, sizeof buf, "%d-wide tiles on %s (%lld units, %lld resident)%s", plan.bn,
+             plan.pair ? "CTA pairs of 256 rows" : "single CTAs of 128 rows", (long long)plan.units,
+             (long long)plan.resident, split > 1 ? ", last wave split along K" : "");
+    std::string r = buf;
+    if (split > 1)
+        r += " " + std::to_string(split) + " ways";
+    return r;
+}
+
 // The dequant kernels by output type, tile mode, K-split and residual.
 template <bool MIXED, bool SPLIT, bool RES>
 static cudaError_t launch_dequant(bool pair, int out_dtype, const CUtensorMap& tmA, const CUtensorMap& tmB,
@@ -1094,24 +1111,13 @@ cudaError_t read_device_error(unsigned int* value, bool clear)
 
 cudaError_t device_error_ptr(unsigned int** ptr)
 {
-    static unsigned int* cached[64] = {};
-    static std::mutex mu;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
+    static ContextCache<unsigned int*> cache;
+    return cache.get(ptr, [](unsigned int** p) {
+        void* a = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&a, g_device_error);
+        *p = static_cast<unsigned int*>(a);
         return e;
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < 64 && cached[dev]) {
-        *ptr = cached[dev];
-        return cudaSuccess;
-    }
-    void* p = nullptr;
-    if ((e = cudaGetSymbolAddress(&p, g_device_error)) != cudaSuccess)
-        return e;
-    if (dev >= 0 && dev < 64)
-        cached[dev] = static_cast<unsigned int*>(p);
-    *ptr = static_cast<unsigned int*>(p);
-    return cudaSuccess;
+    });
 }
 
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s)

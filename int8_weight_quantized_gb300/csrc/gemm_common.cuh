@@ -1,6 +1,6 @@
-// gemm_common.cuh -- pieces shared by the two tcgen05 GEMM kernels (gemm.cu: activation
-// codes as the MMA's A operand; wgemm.cu: the weight converted into tensor memory as A):
-// output types of the dequant epilogue, the bounded teardown wait, the wait limit.
+// gemm_common.cuh -- pieces of the tcgen05 GEMM kernel (gemm.cu) kept apart from its
+// main loop: output types of the dequant epilogue, the bounded teardown wait, the wait
+// limit.
 #pragma once
 
 #include <cstdint>

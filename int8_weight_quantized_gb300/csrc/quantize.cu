@@ -593,7 +593,13 @@ __global__ void __launch_bounds__(256) quant_flat_kernel(const uint4* __restrict
 // round trip after the last block published.  Values left by any earlier launch carry
 // another epoch and are never taken.  The grid never exceeds the number of co-resident
 // blocks (nor kMaxSlotsPerThread * 256), so every block gets to publish; the waits are
-// bounded all the same (a timeout sets `err` and the block goes on).
+// bounded all the same.
+// A block whose wait gives up sets kErrWaitGrid in `err` and makes x_scale NaN, so that
+// every output of the layer is NaN instead of plausible: it first tags the `poison` word
+// with this launch's epoch, then (after an SC fence) stores NaN into x_scale.  Block 0
+// stores the real scale, and at its end (after an SC fence) reads the poison word and
+// stores NaN if it carries this epoch.  Of two SC fences one comes first, so either block
+// 0 sees the tag or its store precedes the NaN store: x_scale ends NaN either way.
 struct alignas(16) EpochSlot {
     unsigned long long epoch;
     float value;
@@ -618,6 +624,21 @@ __device__ __forceinline__ void fence_acq_rel_gpu()
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
+__device__ __forceinline__ void fence_sc_gpu()
+{
+    asm volatile("fence.sc.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_f32(float* p, float v)
+{
+    asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
 // The first `staged` vectors a thread loads in step 1 are also kept in dynamic shared
 // memory (slot j of thread t at [j][t]: conflict-free, only the thread itself reads it
 // back), so step 4 reads them from there instead of from L2 / HBM.
@@ -625,9 +646,9 @@ constexpr int kMaxStagedVectors = 13;  // 13 vectors per thread: 208 KiB of the 
 constexpr int kPrepThreads = 256;      // threads per block
 template <int TPB>
 __global__ void __launch_bounds__(TPB) tensorwise_prep_kernel(
-    const uint4* __restrict__ x, int64_t nvec, EpochSlot* slots, unsigned long long epoch,
-    __nv_bfloat16* __restrict__ q16, float* __restrict__ xs, const uint4* __restrict__ w8, int64_t w_n16,
-    uint4* __restrict__ w16, uint64_t timeout_ns, unsigned int* err, int staged)
+    const uint4* __restrict__ x, int64_t nvec, EpochSlot* slots, unsigned long long* poison,
+    unsigned long long epoch, __nv_bfloat16* __restrict__ q16, float* xs, const uint4* __restrict__ w8,
+    int64_t w_n16, uint4* __restrict__ w16, uint64_t timeout_ns, unsigned int* err, int staged)
 {
     extern __shared__ uint4 x_stage[];
     griddep_wait();
@@ -673,6 +694,7 @@ __global__ void __launch_bounds__(TPB) tensorwise_prep_kernel(
         if ((int)threadIdx.x + TPB * j >= G)
             seen |= 1u << j;
     const uint64_t t0 = globaltimer_ns();
+    bool gave_up = false;  // block-uniform
     for (uint32_t round = 1;; ++round) {
 #pragma unroll
         for (int j = 0; j < kMaxSlotsPerThread; ++j)
@@ -684,6 +706,7 @@ __global__ void __launch_bounds__(TPB) tensorwise_prep_kernel(
         if (__syncthreads_or(give_up)) {
             if (threadIdx.x == 0)
                 atomicOr(err, kErrWaitGrid);
+            gave_up = true;
             break;
         }
         if (__syncthreads_and(seen == (1u << kMaxSlotsPerThread) - 1u))
@@ -703,9 +726,16 @@ __global__ void __launch_bounds__(TPB) tensorwise_prep_kernel(
     float g = 0.0f;
     for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
         g = fmaxf(g, red[i]);
-    const float sc = __fdiv_rn(g, 127.0f);
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-        xs[0] = sc;
+    const float sc = gave_up ? __int_as_float(0x7FFFFFFF) : __fdiv_rn(g, 127.0f);
+    if (threadIdx.x == 0) {
+        if (gave_up) {
+            st_relaxed_u64(poison, epoch);
+            fence_sc_gpu();
+            st_relaxed_f32(xs, sc);
+        } else if (blockIdx.x == 0) {
+            st_relaxed_f32(xs, sc);
+        }
+    }
     // 4. quantize this block's slice
     const Quantizer qz(sc, false);
     slot = 0;
@@ -730,6 +760,11 @@ __global__ void __launch_bounds__(TPB) tensorwise_prep_kernel(
                 store8<false, true>(qv, nullptr, q16, i * 8);
             }
         }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && !gave_up) {
+        fence_sc_gpu();
+        if (ld_relaxed_u64(poison) == epoch)
+            st_relaxed_f32(xs, __int_as_float(0x7FFFFFFF));
     }
 }
 
@@ -936,26 +971,24 @@ cudaError_t launch_prep_rows(const void* x, int64_t M, int64_t K, bool rotate, v
 
 namespace {
 
-// Blocks of tensorwise_prep_kernel that are resident at once on the whole device.
+// Blocks of tensorwise_prep_kernel that are resident at once on the whole device (the
+// shared-memory attribute it needs is set once per context).
 int prep_capacity(const DeviceInfo& dev)
 {
-    static int cached[64] = {};
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
-    int& c = cached[(dev.device >= 0 && dev.device < 64) ? dev.device : 0];
-    if (c == 0) {
-        int per_sm = 0;
+    static ContextCache<int> cache;
+    int per_sm = 0;
+    const cudaError_t e = cache.get(&per_sm, [](int* n) {
         constexpr int TPB = quant::kPrepThreads;
         const size_t smem = (size_t)quant::kMaxStagedVectors * TPB * sizeof(uint4);
-        if (cudaFuncSetAttribute(quant::tensorwise_prep_kernel<TPB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant::tensorwise_prep_kernel<TPB>, TPB, smem) !=
-                cudaSuccess ||
-            per_sm <= 0)
-            per_sm = 1;
-        c = per_sm * dev.sm_count;
-    }
-    return c;
+        cudaError_t r = cudaFuncSetAttribute(quant::tensorwise_prep_kernel<TPB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (r == cudaSuccess)
+            r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, quant::tensorwise_prep_kernel<TPB>, TPB, smem);
+        return r;
+    });
+    if (e != cudaSuccess || per_sm <= 0)
+        per_sm = 1;
+    return per_sm * dev.sm_count;
 }
 
 // A 64-bit value no earlier launch of this process used (high-entropy start, so values
@@ -980,7 +1013,8 @@ unsigned long long next_prep_epoch()
 
 size_t prep_tensorwise_scratch_bytes(int max_blocks)
 {
-    return sizeof(quant::EpochSlot) * (size_t)max_blocks;
+    // one slot per block, then the poison word of a wait that gave up
+    return sizeof(quant::EpochSlot) * ((size_t)max_blocks + 1);
 }
 
 cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q16, float* x_scale, void* scratch,
@@ -1016,8 +1050,9 @@ cudaError_t launch_prep_tensorwise(const void* x, int64_t M, int64_t K, void* q1
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, quant::tensorwise_prep_kernel<TPB>, static_cast<const uint4*>(x), nvec,
-                              static_cast<quant::EpochSlot*>(scratch), next_prep_epoch(),
+    quant::EpochSlot* slots = static_cast<quant::EpochSlot*>(scratch);
+    return cudaLaunchKernelEx(&cfg, quant::tensorwise_prep_kernel<TPB>, static_cast<const uint4*>(x), nvec, slots,
+                              &slots[max_blocks].epoch, next_prep_epoch(),
                               static_cast<__nv_bfloat16*>(q16), x_scale, reinterpret_cast<const uint4*>(w8),
                               w_n >> 4, static_cast<uint4*>(w16), (uint64_t)2000000000ull, err, staged);
 }

@@ -1,6 +1,8 @@
 """GPU parity of the tensor-core GEMM: raw int32 accumulators bit-exact against the
 oracle (including adversarial inputs that stress the exact-fp32-chunk argument), and
-the fused dequant epilogue within 1 bf16 ulp of the oracle's."""
+the fused dequant epilogue bit-identical to the oracle's (0 ulp in every output type).
+Outputs and workspaces sit between guard bands pre-filled with values the kernels never
+write, so a skipped tile or a stray write fails the test."""
 import numpy as np
 import pytest
 import torch
@@ -8,15 +10,25 @@ import torch
 import oracle
 import int8_weight_quantized_gb300 as ck
 from int8_weight_quantized_gb300 import synthetic
-from helpers import bits, bf16_ulp_distance, out_bits, ulp_distance, MAX_ULP
+from helpers import (bits, bf16_ulp_distance, out_bits, ulp_distance, MAX_ULP, guarded, assert_guards_intact,
+                     assert_all_written, guarded_workspace, assert_workspace_guards_intact, NAN16, NAN32, ACC_NEVER)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
 def gpu_acc(q, w):
-    acc = ck.ck_int8_gemm_s32(q.to(DEV), w.to(DEV))
+    """The raw accumulators, written between guard bands of a value no exact accumulator
+    can take (INT32_MIN), with a guard-banded workspace of random bytes."""
+    M, K = q.shape
+    N = w.shape[0]
+    abuf, acc = guarded((M, N), torch.int32, ACC_NEVER)
+    wbuf, ws, before = guarded_workspace(ck.load_library().ck_int8_gemm_workspace_size(M, N, K), seed=M + N)
+    ck.ck_int8_gemm_s32(q.to(DEV), w.to(DEV), acc=acc, ws=ws)
     torch.cuda.synchronize()
+    assert_guards_intact(abuf, ACC_NEVER)
+    assert_all_written(abuf, ACC_NEVER)
+    assert_workspace_guards_intact(wbuf, before)
     return acc.cpu().numpy()
 
 
@@ -77,9 +89,12 @@ def test_dequant_parity(M, N, K, scalar, with_bias):
     b = synthetic.normal_bf16((1, N), seed=15, std=0.5).reshape(N) if with_bias else None
     acc = oracle.gemm_s32(q.numpy(), w.numpy())
     ref = oracle.dequant(acc, xs.numpy(), ws.numpy(), None if b is None else bits(b), scalar_scales=scalar)
-    y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), None if b is None else b.to(DEV),
-                                scalar_scales=scalar)
+    ybuf, y = guarded((M, N), torch.bfloat16, NAN16)
+    ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), None if b is None else b.to(DEV),
+                            scalar_scales=scalar, y=y)
     torch.cuda.synchronize()
+    assert_guards_intact(ybuf, NAN16)
+    assert_all_written(ybuf, NAN16)
     d = bf16_ulp_distance(bits(y), ref)
     assert d.max() <= MAX_ULP, "max ulp %d at %s" % (d.max(), np.unravel_index(d.argmax(), d.shape))
 
@@ -127,16 +142,20 @@ def typed_reference(q, w, xs, ws, b, scalar, code):
 @pytest.mark.parametrize("M,N,K", [(256, 512, 512), (129, 264, 1040), (1, 8, 16), (385, 520, 192)])
 def test_dequant_output_types(M, N, K, scalar, with_bias, out_dtype, code):
     """The epilogue's fp32 value rounded to fp16 / stored as fp32 (the out_dtype of
-    int8_linear): within 1 ulp of the oracle in that type."""
+    int8_linear): bit-identical to the oracle in that type."""
     q = synthetic.int8_uniform((M, K), seed=21 + M)
     w = synthetic.int8_uniform((N, K), seed=22 + N)
     xs = synthetic.scale_uniform(1 if scalar else M, seed=23, mul=0.02)
     ws = synthetic.scale_uniform(1 if scalar else N, seed=24, mul=0.01)
     b = synthetic.normal_bf16((1, N), seed=25, std=0.5).reshape(N) if with_bias else None
     ref = typed_reference(q, w, xs, ws, b, scalar, code)
-    y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), None if b is None else b.to(DEV),
-                                scalar_scales=scalar, out_dtype=out_dtype)
+    pattern = NAN32 if out_dtype == torch.float32 else NAN16
+    ybuf, y = guarded((M, N), out_dtype, pattern)
+    ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), None if b is None else b.to(DEV),
+                            scalar_scales=scalar, out_dtype=out_dtype, y=y)
     torch.cuda.synchronize()
+    assert_guards_intact(ybuf, pattern)
+    assert_all_written(ybuf, pattern)
     assert y.dtype == out_dtype
     d = ulp_distance(out_bits(y), ref)
     assert d.max() <= MAX_ULP, "max ulp %d at %s" % (d.max(), np.unravel_index(d.argmax(), d.shape))
@@ -170,8 +189,11 @@ def test_f32_output_every_tile_width(monkeypatch, bn):
     ws = synthetic.scale_uniform(N, seed=44, mul=0.01)
     b = synthetic.normal_bf16((1, N), seed=45, std=0.5).reshape(N)
     ref = typed_reference(q, w, xs, ws, b, False, oracle.OUT_F32)
-    y = ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), out_dtype=torch.float32)
+    ybuf, y = guarded((M, N), torch.float32, NAN32)
+    ck.ck_int8_gemm_dequant(q.to(DEV), xs.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), out_dtype=torch.float32, y=y)
     torch.cuda.synchronize()
+    assert_guards_intact(ybuf, NAN32)
+    assert_all_written(ybuf, NAN32)
     assert ulp_distance(out_bits(y), ref).max() <= MAX_ULP
 
 
@@ -191,9 +213,14 @@ def test_tile_config_query(monkeypatch):
 
 
 def run_s32(q, w, ws=None):
-    acc = ck.ck_int8_gemm_s32(q.to(DEV), w.to(DEV), ws=ws)
+    M, K = q.shape
+    N = w.shape[0]
+    abuf, acc = guarded((M, N), torch.int32, ACC_NEVER)
+    ck.ck_int8_gemm_s32(q.to(DEV), w.to(DEV), acc=acc, ws=ws)
     torch.cuda.synchronize()
     assert ck.ck_device_error(clear=False) == 0
+    assert_guards_intact(abuf, ACC_NEVER)
+    assert_all_written(abuf, ACC_NEVER)
     return acc.cpu().numpy()
 
 
@@ -212,10 +239,13 @@ def test_split_tail_exact(monkeypatch, M, N, K, pair, split):
     q = synthetic.int8_uniform((M, K), seed=M + 3)
     w = synthetic.int8_uniform((N, K), seed=N + 4)
     ref = oracle.gemm_s32(q.numpy(), w.numpy())
+    # the slices' int32 partial sums and arrival slots live in the workspace: guard-banded
+    wbuf, ws, before = guarded_workspace(ck.load_library().ck_int8_gemm_workspace_size(M, N, K), seed=M + K)
     for _ in range(2):  # the second launch finds the first one's arrival slots
-        got = run_s32(q, w)
+        got = run_s32(q, w, ws=ws)
         bad = np.argwhere(got != ref)
         assert bad.size == 0, "%d mismatches, first at %s" % (len(bad), bad[0])
+        assert_workspace_guards_intact(wbuf, before)
 
 
 def test_split_tail_after_full_waves(monkeypatch):
@@ -255,7 +285,7 @@ def test_split_tail_ignores_stale_workspace(monkeypatch):
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 def test_split_tail_dequant(monkeypatch, out_dtype):
-    """The fused epilogue after a K-split: within 1 ulp of the oracle, as without it."""
+    """The fused epilogue after a K-split: bit-identical to the oracle, as without it."""
     monkeypatch.setenv("CK_GEMM_SPLIT", "3")
     M, N, K = 512, 1024, 2048
     q = synthetic.int8_uniform((M, K), seed=61)

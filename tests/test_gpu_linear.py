@@ -1,7 +1,9 @@
 """The whole layer, ck_int8_linear, on the workloads of the comfy-kitchen pages, against
-the CPU oracle: full outputs where the oracle finishes in seconds, seeded row samples
-(plus the first and last 16 rows) on the multi-GB shapes, including the M*N >= 2^31
-boundary of issue #136."""
+the CPU oracle, bit for bit: full outputs where the oracle finishes in seconds, seeded row
+samples (plus the first and last 16 rows) on the multi-GB shapes, including the
+M*N >= 2^31 boundary of issue #136.  Every output is written into a buffer pre-filled with
+NaN between two guard bands: after the call no element may still be NaN (every tile was
+written, at its own address) and the bands must be untouched."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +11,8 @@ import torch
 import oracle
 import int8_weight_quantized_gb300 as ck
 from int8_weight_quantized_gb300 import synthetic
-from helpers import bits, bf16_ulp_distance, out_bits, ulp_distance, MAX_ULP
+from helpers import (bits, bf16_ulp_distance, out_bits, ulp_distance, MAX_ULP, guarded, assert_guards_intact,
+                     assert_all_written, NAN16, NAN32)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -28,8 +31,11 @@ def run_full(spec):
         w, ws = case.w, case.w_scale
     b = case.bias
     ref = oracle.int8_linear(bits(case.x), w.numpy(), ws.numpy(), None if b is None else bits(b), mode=case.mode)
-    y = ck.ck_int8_linear(case.x.to(DEV), w.to(DEV), ws.to(DEV), None if b is None else b.to(DEV), mode=case.mode)
+    ybuf, y = guarded((case.M, case.N), torch.bfloat16, NAN16)
+    ck.ck_int8_linear(case.x.to(DEV), w.to(DEV), ws.to(DEV), None if b is None else b.to(DEV), mode=case.mode, y=y)
     torch.cuda.synchronize()
+    assert_guards_intact(ybuf, NAN16)
+    assert_all_written(ybuf, NAN16)
     d = bf16_ulp_distance(bits(y), ref["y"])
     assert d.max() <= MAX_ULP, "%s: max ulp %d at %s" % (spec[0], d.max(), np.unravel_index(d.argmax(), d.shape))
     return case, y
@@ -55,8 +61,12 @@ def test_output_types(mode, out_dtype, code):
     ref = oracle.int8_linear(bits(x), w.numpy(), ws.numpy(), bits(b), mode=mode, out_dtype=code)["y"]
     if code == oracle.OUT_F32:
         ref = ref.view(np.uint32)
-    y = ck.ck_int8_linear(x.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), mode=mode, out_dtype=out_dtype)
+    pattern = NAN32 if code == oracle.OUT_F32 else NAN16
+    ybuf, y = guarded((M, N), out_dtype, pattern)
+    ck.ck_int8_linear(x.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), mode=mode, out_dtype=out_dtype, y=y)
     torch.cuda.synchronize()
+    assert_guards_intact(ybuf, pattern)
+    assert_all_written(ybuf, pattern)
     assert y.dtype == out_dtype
     d = ulp_distance(out_bits(y), ref)
     assert d.max() <= MAX_ULP, "max ulp %d at %s" % (d.max(), np.unravel_index(d.argmax(), d.shape))
@@ -79,24 +89,35 @@ def test_sweep_small_shapes_full(spec):
     run_full(spec)
 
 
+def boundary_rows(M, N):
+    """The rows around the int32 element-offset limit: row r holds elements r*N ..
+    r*N + N - 1, so the row that crosses 2^31 and its neighbours (issue #136, "Summary")."""
+    r = (2 ** 31) // N
+    return [i for i in (r - 1, r, r + 1) if 0 <= i < M]
+
+
 def run_sampled(spec):
     name, M, N, K, mode, bias, frac, seed = spec
     # the activation is drawn on the GPU (multi-GB); the weight on the CPU, as the oracle needs all of it
     x = synthetic.normal_bf16((M, K), seed, device=DEV)
     w = synthetic.int8_uniform((N, K), seed + 101)
     ws = synthetic.scale_uniform(N, seed + 202)
-    y = ck.ck_int8_linear(x, w.to(DEV), ws.to(DEV), None, mode=mode)
+    # y inside a NaN-filled buffer with guard bands: every one of the M*N outputs must be
+    # overwritten with a finite value, nothing written outside
+    ybuf, y = guarded((M, N), torch.bfloat16, NAN16)
+    ck.ck_int8_linear(x, w.to(DEV), ws.to(DEV), None, mode=mode, y=y)
     torch.cuda.synchronize()
-    rows = synthetic.sample_rows(M, seed=1000 + seed)
+    assert_guards_intact(ybuf, NAN16)
+    for r0 in range(0, M, 8192):
+        assert bool(torch.isfinite(y[r0:r0 + 8192]).all()), "%s: a non-finite output in rows %d.." % (name, r0)
+    rows = sorted(set(synthetic.sample_rows(M, seed=1000 + seed)) | set(boundary_rows(M, N)))
     idx = torch.tensor(rows, device=DEV)
     xr = bits(x.index_select(0, idx))
     ref = oracle.int8_linear(xr, w.numpy(), ws.numpy(), None, mode=mode)
     got = bits(y.index_select(0, idx))
     d = bf16_ulp_distance(got, ref["y"])
     assert d.max() <= MAX_ULP, "%s: max ulp %d at sample row %d" % (name, d.max(), rows[int(d.max(axis=1).argmax())])
-    # every row was written (no wrapped or skipped tile): finite values only
-    assert torch.isfinite(y[-1]).all() and torch.isfinite(y[0]).all()
-    del x, y
+    del x, y, ybuf
     torch.cuda.empty_cache()
 
 
@@ -110,6 +131,8 @@ def test_sweep_large_shapes_sampled(spec):
 @pytest.mark.parametrize("spec", synthetic.LARGE_INDEX, ids=lambda s: s[0])
 def test_large_index_boundary_sampled(spec):
     assert spec[1] * spec[2] >= 2 ** 31 - 21504  # straddles the int32 element-offset limit
+    M, N = spec[1], spec[2]
+    assert boundary_rows(M, N)[-1] == min(M - 1, 2 ** 31 // N + 1)  # the sample includes the crossing row
     run_sampled(spec)
 
 
@@ -129,8 +152,10 @@ def test_linear_residual_in_place(mode):
     ref8 = oracle.int8_linear(bits(x), w.numpy(), ws.numpy(), bits(b), mode=mode)
     ref = oracle.dequant_residual(ref8["acc"], ref8["xs"], ws.numpy(), r.float().numpy(), bits(b),
                                   scalar_scales=(mode == synthetic.TENSORWISE))
-    y = r.to(DEV)
+    ybuf, y = guarded((M, N), torch.bfloat16, NAN16)
+    y.copy_(r.to(DEV))
     ck.ck_int8_linear(x.to(DEV), w.to(DEV), ws.to(DEV), b.to(DEV), mode=mode, y=y, residual=y)
     torch.cuda.synchronize()
+    assert_guards_intact(ybuf, NAN16)
     d = bf16_ulp_distance(bits(y), ref)
     assert d.max() <= MAX_ULP, "max ulp %d" % d.max()

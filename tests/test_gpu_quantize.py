@@ -7,16 +7,26 @@ import torch
 import oracle
 import int8_weight_quantized_gb300 as ck
 from int8_weight_quantized_gb300 import synthetic
-from helpers import bits, from_bits
+from helpers import (bits, from_bits, guarded, assert_guards_intact, assert_all_written, CODE_NEVER, NAN32)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
 def check_rowwise(x_cpu, rotate):
+    """Codes and scales written into guard-banded buffers pre-filled with values the
+    quantize never produces (code -128, NaN scales): every element must be written, none
+    outside, and all of them equal to the oracle's."""
     q_ref, s_ref = oracle.quantize_rowwise(bits(x_cpu), rotate=rotate)
-    q, s = ck.ck_quantize_int8_rowwise(x_cpu.to(DEV), rotate=rotate)
+    M, K = x_cpu.shape
+    qbuf, q = guarded((M, K), torch.int8, CODE_NEVER)
+    sbuf, s = guarded((M,), torch.float32, NAN32)
+    ck.ck_quantize_int8_rowwise(x_cpu.to(DEV), rotate=rotate, q=q, x_scale=s)
     torch.cuda.synchronize()
+    assert_guards_intact(qbuf, CODE_NEVER)
+    assert_guards_intact(sbuf, NAN32)
+    assert_all_written(qbuf, CODE_NEVER)
+    assert_all_written(sbuf, NAN32)
     s_np = s.cpu().numpy()
     assert np.array_equal(s_np.view(np.uint32), s_ref.view(np.uint32)), "x_scale differs"
     qn = q.cpu().numpy()
@@ -85,8 +95,13 @@ def test_zero_and_subnormal_rows():
 def test_tensorwise_parity(M, K):
     x = synthetic.normal_bf16((M, K), seed=300 + K)
     q_ref, s_ref = oracle.quantize_tensorwise(bits(x))
-    q, s = ck.ck_quantize_int8_tensorwise(x.to(DEV))
+    qbuf, q = guarded((M, K), torch.int8, CODE_NEVER)
+    sbuf, s = guarded((1,), torch.float32, NAN32)
+    ck.ck_quantize_int8_tensorwise(x.to(DEV), q=q, x_scale=s)
     torch.cuda.synchronize()
+    assert_guards_intact(qbuf, CODE_NEVER)
+    assert_guards_intact(sbuf, NAN32)
+    assert_all_written(qbuf, CODE_NEVER)
     assert s.cpu().numpy().view(np.uint32)[0] == s_ref.view(np.uint32)[0]
     assert np.array_equal(q.cpu().numpy(), q_ref)
 

@@ -136,3 +136,22 @@ def test_tile_config_query_validates_without_a_gpu(lib):
     st = lib.ck_gemm_tile_config(16, 16, 32, ctypes.byref(bn), ctypes.byref(pair), None, None)
     if not torch.cuda.is_available():
         assert st in (ck.CK_ERR_CUDA, ck.CK_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_workspace_views(lib):
+    """Where the layer leaves its activation codes and scales: the codes first, x_scale
+    after the bf16 activation and weight operands, both inside the workspace and aligned;
+    bad arguments are rejected."""
+    import ctypes
+    import int8_weight_quantized_gb300 as ck
+    for M, N, K, mode in [(4096, 4096, 4096, ck.TENSORWISE), (300, 264, 1152, ck.PER_ROW),
+                          (4096, 12288, 3072, ck.CONVROT), (1, 8, 16, ck.TENSORWISE)]:
+        co, xo = ck.ck_int8_linear_workspace_views(M, N, K, mode)
+        size = lib.ck_int8_linear_workspace_size(M, N, K, mode)
+        n_scales = 1 if mode == ck.TENSORWISE else M
+        assert co == 0 and co + 2 * M * K <= xo
+        assert xo >= 2 * M * K + 2 * N * K and xo % 256 == 0
+        assert xo + 4 * n_scales <= size
+    sz = ctypes.c_size_t()
+    assert lib.ck_int8_linear_workspace_views(16, 8, 16, 7, ctypes.byref(sz), ctypes.byref(sz)) == ck.CK_ERR_INVALID_ARG
+    assert lib.ck_int8_linear_workspace_views(16, 8, 16, 1, None, ctypes.byref(sz)) == ck.CK_ERR_INVALID_ARG
