@@ -29,7 +29,7 @@
  *   - int64 addressing: issue #136 "INT8 GEMM kernels index the output in int32:
  *     illegal memory access once m*n >= 2**31", sections "Summary" and "Suggested fix".
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent:
  *   R1 rint is round-half-to-even (nearbyintf in the default FE_TONEAREST mode).
  *   R2 v / x_scale is one IEEE fp32 division (not a multiply by a reciprocal).
  *   R3 a row whose x_scale is 0 (all zeros, or amax so small that amax/127 underflows)
@@ -404,7 +404,7 @@ int ck_oracle_prepare_convrot_weight(const float *W, int64_t N, int64_t K, int8_
  * dequantize the INT8 weight on the fly and run the GEMM on 16-bit tensor cores; the
  * stored weight keeps its INT8 footprint; for ConvRot the activation is rotated online,
  * x_rot = x @ H, the GEMM runs in the rotated basis and the weight is not rotated back).
- * Readings (also in the design notes):
+ * Readings where the pages are silent:
  *   R12 the activation is not quantized: a = x as given (bf16), or for ConvRot
  *       a = bf16_rne(x @ H) with the fp32 block transform of R5 (16-bit tensor-core
  *       operands hold bf16, so the rotated activation is rounded once);

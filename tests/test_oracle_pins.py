@@ -536,3 +536,88 @@ def test_residual_within_rounding_of_the_exact_value():
             exact = prod + Fraction(float(bf[n])) + Fraction(float(r[m, n]))
             bound = (abs(prod) + abs(Fraction(float(bf[n]))) + abs(Fraction(float(r[m, n])))) * Fraction(4, 2 ** 24)
             assert abs(Fraction(float(y[m, n])) - exact) <= bound
+
+
+# ---------------------------------------------------------------- epilogue operation order
+def _rne_f32_bits(v):
+    """Exact rational -> fp32 bits, round to nearest even (normal numbers only), written
+    out from the format's definition: 24 significant bits, exponent bias 127."""
+    if v == 0:
+        return 0
+    sign = 0x80000000 if v < 0 else 0
+    a = abs(Fraction(v))
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    m = a / Fraction(2) ** (e - 23)          # in [2^23, 2^24)
+    fl = m.numerator // m.denominator
+    rem = m - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    if fl == 1 << 24:
+        fl >>= 1
+        e += 1
+    assert -126 <= e <= 127
+    return sign | ((e + 127) << 23) | (fl - (1 << 23))
+
+
+def _f32_value(b):
+    """fp32 bits -> exact rational (normal numbers)."""
+    e = ((b >> 23) & 0xFF) - 127
+    m = (b & 0x7FFFFF) | (1 << 23)
+    v = Fraction(m) * Fraction(2) ** (e - 23)
+    return -v if b & 0x80000000 else v
+
+
+def _bf16_value(b):
+    return _f32_value(b << 16)
+
+
+def _read_epilogue_examples():
+    rows = []
+    with open(os.path.join(GOLDEN, "epilogue_order_examples.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            acc, xs, ws, bias, want, other = [p.strip() for p in line.split("|")]
+            rows.append((int(acc), int(xs, 16), int(ws, 16), None if bias == "-" else int(bias, 16), int(want, 16),
+                         int(other, 16)))
+    return rows
+
+
+def test_epilogue_order_worked_examples():
+    """The hand-derived examples of tests/golden/epilogue_order_examples.txt: the oracle's
+    epilogue gives the left-to-right bits, which exact rational arithmetic confirms step by
+    step; the contrasting evaluation (another multiplication order, or an FMA for the bias
+    add) gives the other bits, so a change of order in the oracle would fail here."""
+    rows = _read_epilogue_examples()
+    assert len(rows) == 2
+    for acc, xs_b, ws_b, bias_b, want, other in rows:
+        xs, ws = _f32_value(xs_b), _f32_value(ws_b)
+        t1 = _rne_f32_bits(acc * xs)
+        t2 = _rne_f32_bits(_f32_value(t1) * ws)
+        if bias_b is None:
+            left = t2
+            alt = _rne_f32_bits(acc * _f32_value(_rne_f32_bits(xs * ws)))          # acc * (xs * ws)
+            alt2 = _rne_f32_bits(_f32_value(_rne_f32_bits(acc * ws)) * xs)         # (acc * ws) * xs
+            assert alt == alt2 == other
+        else:
+            left = _rne_f32_bits(_f32_value(t2) + _bf16_value(bias_b))
+            alt = _rne_f32_bits(_f32_value(t1) * ws + _bf16_value(bias_b))        # fused multiply-add
+            assert alt == other
+        assert left == want and want != other
+        got = oracle.dequant_typed(np.array([[acc]], np.int32), np.array([xs_b], np.uint32).view(np.float32),
+                                   np.array([ws_b], np.uint32).view(np.float32),
+                                   None if bias_b is None else np.array([bias_b], np.uint16),
+                                   out_dtype=oracle.OUT_F32)
+        assert int(got.view(np.uint32)[0, 0]) == want, "oracle epilogue gave %#x, expected %#x" % (
+            int(got.view(np.uint32)[0, 0]), want)
+        # the same value through the tensorwise (scalar-scale) form of the epilogue
+        got_s = oracle.dequant_typed(np.array([[acc]], np.int32), np.array([xs_b], np.uint32).view(np.float32),
+                                     np.array([ws_b], np.uint32).view(np.float32),
+                                     None if bias_b is None else np.array([bias_b], np.uint16),
+                                     scalar_scales=True, out_dtype=oracle.OUT_F32)
+        assert int(got_s.view(np.uint32)[0, 0]) == want
