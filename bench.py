@@ -46,6 +46,7 @@ WORKLOADS = {spec[0]: spec for spec in synthetic.ALL_WORKLOADS}
 DEFAULT_WORKLOAD = synthetic.SWEEP[-1][0]  # per_row_80666x28672x5376
 TIMED_SECONDS = 8.0  # target length of the timed region when --steps is not given
 FLUSH_BYTES = 512 << 20  # > 129 MB of L2: written between steps (outside the timed events)
+L2_BYTES = 129 << 20
 CLEAN_BYTES = 256 << 20  # then read, so the step does not start by writing back the flush's dirty lines
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 GEMM_SOURCES = ["int8_weight_quantized_gb300/csrc/gemm.cu", "int8_weight_quantized_gb300/csrc/ck_device.cuh",
@@ -422,7 +423,7 @@ def run_ours(args, spec):
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int8" if not w8a16 else "bf16", "data": "synthetic",
             "config": workload_config(spec, "flushed between steps (%d MiB write, then %d MiB read); inputs %s L2" % (
-                FLUSH_BYTES >> 20, CLEAN_BYTES >> 20, "larger than" if M * K * 2 > (129 << 20) else "smaller than")),
+                FLUSH_BYTES >> 20, CLEAN_BYTES >> 20, "larger than" if M * K * 2 > L2_BYTES else "smaller than")),
             "roofline": roofline, "kernels": kernels, "e2e": e2e, "clocks": clocks,
             "gpu_launches": int(sum(n for _, n in counts.values())), "timed_wall_s": wall}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -437,7 +438,9 @@ def run_ours(args, spec):
 def time_quantize_int8(ck, x, mode, flush_l2, n, hbm_peak, dev):
     """The stand-alone activation quantize (ck_quantize_int8_rowwise, rotated for ConvRot,
     or ck_quantize_int8_tensorwise): bf16 x in, int8 codes and fp32 scales out, each launch
-    bracketed by CUDA events on the launching stream, L2 flushed before it."""
+    bracketed by CUDA events on the launching stream.  L2 is flushed before each launch
+    unless x alone is larger than L2 (then launches follow each other, as in a stream of
+    calls, and no launch finds its input in L2)."""
     M, K = x.shape
     tw = mode == synthetic.TENSORWISE
     q = torch.empty((M, K), dtype=torch.int8, device=dev)
@@ -453,9 +456,11 @@ def time_quantize_int8(ck, x, mode, flush_l2, n, hbm_peak, dev):
         flush_l2(i)
         run()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    flush = 2 * M * K <= L2_BYTES
     torch.cuda.synchronize()
     for i, (e0, e1) in enumerate(evs):
-        flush_l2(i)
+        if flush:
+            flush_l2(i)
         e0.record()
         run()
         e1.record()
@@ -464,7 +469,8 @@ def time_quantize_int8(ck, x, mode, flush_l2, n, hbm_peak, dev):
     nbytes = (5 * M * K + 4) if tw else (3 * M * K + 4 * M)
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"entry": "ck_quantize_int8_tensorwise" if tw else "ck_quantize_int8_rowwise",
-            "rotate": mode == synthetic.CONVROT, "ms": ms, "launches": n, "bytes_algorithmic": nbytes,
+            "rotate": mode == synthetic.CONVROT, "ms": ms, "launches": n, "l2_flushed": flush,
+            "bytes_algorithmic": nbytes,
             "GB/s": gbs, "frac_hbm": gbs / hbm_peak, "peak_hbm_gbs": hbm_peak}
 
 

@@ -1,6 +1,6 @@
 // quantize.cu -- activation quantize kernels (per-row, tensorwise, ConvRot-rotated)
 // and the int8 -> bf16 widening of tensor-core operands.  All are HBM-bandwidth bound:
-// 16-byte vector loads, warp-shuffle reductions, no shared-memory staging needed.
+// 16-byte vector loads straight into registers, warp-shuffle reductions.
 //
 // What they compute (comfy-kitchen issue #278, quantize_int8_rowwise, and issue #280,
 // tensor-wide scales):
@@ -14,8 +14,12 @@
 //   t = v * r;  e = fma(-t, s, v)  (exact remainder);  t = fma(e, r, t)
 // which equals the IEEE quotient; this was checked exhaustively on the CPU for every
 // pair of bf16 significands (numerator <= maximum) over the full exponent range that
-// can reach rint's decision, with zero mismatches.  Rows with a tiny scale
-// (s < 2^-100) and every ConvRot row (fp32 v) use the IEEE division itself.
+// can reach rint's decision, with zero mismatches.  ConvRot values are fp32: there the
+// product v * r decides the code wherever a rigorous error bound shows it must agree
+// with the IEEE quotient, and the IEEE division settles the rest (see Coder).  Scales
+// below 2^-100 use the IEEE division throughout.  x_scale itself is fl(amax / 127) by a
+// correction sequence checked exhaustively (div127), and the rounding to an integer is an
+// fp32 add (kRoundMagic): no step needs the quarter-rate conversion instructions.
 #include <algorithm>
 #include <atomic>
 #include <chrono>
@@ -66,79 +70,157 @@ __device__ __forceinline__ __nv_bfloat162 absmax8(__nv_bfloat162 m, const uint4&
     return m;
 }
 
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8])
+// Rounding without the conversion pipe.  For |t| < 2^22, t + 1.5 * 2^23 lands in
+// [2^23, 2^24), where the fp32 spacing is 1, so the add rounds t to an integer (half to
+// even) and leaves it in the low mantissa bits: the low byte of the sum's bits is that
+// integer's int8 two's-complement byte, and subtracting 1.5 * 2^23 again gives it back as
+// an exact float.  A bf16 value of an integer |q| <= 127 (at most 7 significant bits) is
+// the upper half of q's fp32 bits, without rounding.  This keeps the quantize off the
+// quarter-rate conversion instructions, which at HBM speed would be its bottleneck.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+
+// x_scale = fl(amax / 127) for amax >= 0 finite, without a division: q1 = fl(amax * c)
+// with c = fl(1/127), then one FMA correction of the remainder (Markstein, IBM J. Res.
+// Dev. 34(1), 1990).  The result equals the correctly rounded quotient for every
+// non-negative finite fp32 amax: checked exhaustively on the CPU (all 2^31 - 2^23 of
+// them, against the exact remainder amax - 127 * s), and on the GPU for every bf16 amax.
+__device__ __forceinline__ float div127(float amax)
 {
-    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __low2float(p[i]);
-        f[2 * i + 1] = __high2float(p[i]);
-    }
+    const float c = 0x1.020408p-7f;  // fl(1/127), bits 0x3C010204
+    const float q1 = __fmul_rn(amax, c);
+    const float e = __fmaf_rn(-q1, 127.0f, amax);
+    return __fmaf_rn(e, c, q1);
 }
 
-// The per-element rule with scale s.  kind: 0 -> scale is zero (q = 0),
-// 1 -> reciprocal + Markstein correction, 2 -> IEEE division.
-struct Quantizer {
+// One code, as the magic sum (t rounded + kRoundMagic), by the scale's rule:
+//   kind 1 (bf16 v, scale >= 2^-100): the reciprocal and Markstein correction give the
+//     IEEE quotient; with s = fl(amax / 127) normal, |v / s| <= 127 (1 + 2^-23), whose rint
+//     is 127, so no clamp is needed;
+//   kind 3 (fp32 v of ConvRot, scale >= 2^-100): t = v * fl(1/s) is within 2^-16 of v / s
+//     (two roundings of a quotient below 128) and the IEEE quotient within 2^-18 of it,
+//     so where t is more than 2^-14 away from a half-integer both round to the same
+//     integer; nearer than that (about 1 value in 16000) the IEEE quotient is formed;
+//   kind 2 (scales below 2^-100): the IEEE quotient, clamped;  kind 0: code 0.
+struct Coder {
     float s, r;
     int kind;
-    __device__ __forceinline__ explicit Quantizer(float s_, bool exact_div_only)
+    __device__ __forceinline__ Coder(float s_, bool fp32_values)
     {
         s = s_;
         r = 0.0f;
         if (s_ == 0.0f) {
             kind = 0;
-        } else if (!exact_div_only && s_ >= 0x1p-100f) {
-            kind = 1;
-            r = __fdiv_rn(1.0f, s_);
+        } else if (s_ >= 0x1p-100f) {
+            kind = fp32_values ? 3 : 1;
+            r = __frcp_rn(s_);  // correctly rounded 1 / s
         } else {
             kind = 2;
         }
     }
+    __device__ __forceinline__ float slow(float v) const
+    {
+        return __fadd_rn(fminf(fmaxf(rintf(__fdiv_rn(v, s)), -127.0f), 127.0f), kRoundMagic);
+    }
+    __device__ __forceinline__ float magic1(float v) const
+    {
+        float t = __fmul_rn(v, r);
+        const float e = __fmaf_rn(-t, s, v);
+        t = __fmaf_rn(e, r, t);
+        return __fadd_rn(t, kRoundMagic);
+    }
+    __device__ __forceinline__ float magic3(float v) const
+    {
+        const float t = __fmul_rn(v, r);
+        const float m = __fadd_rn(t, kRoundMagic);
+        const float d = __fsub_rn(t, __fsub_rn(m, kRoundMagic));
+        return fabsf(__fsub_rn(fabsf(d), 0.5f)) <= 0x1p-14f ? slow(v) : m;
+    }
+    __device__ __forceinline__ float magic(float v) const
+    {
+        if (kind == 1)
+            return magic1(v);
+        if (kind == 3)
+            return magic3(v);
+        if (kind == 2)
+            return slow(v);
+        return kRoundMagic;
+    }
 };
 
-// Eight values at once, the method chosen once for all eight (the choice is uniform per row).
-__device__ __forceinline__ void quantize8(const Quantizer& qz, const float (&f)[8], float (&qv)[8])
+// Eight codes from eight magic sums: int8 bytes, or bf16 codes.
+template <bool OUT8>
+__device__ __forceinline__ void store_magic8(const float (&m)[8], int8_t* q8, __nv_bfloat16* q16, int64_t off)
 {
-    if (qz.kind == 1) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float t = __fmul_rn(f[i], qz.r);
-            const float e = __fmaf_rn(-t, qz.s, f[i]);
-            t = __fmaf_rn(e, qz.r, t);
-            qv[i] = fminf(fmaxf(rintf(t), -127.0f), 127.0f);
-        }
-    } else if (qz.kind == 2) {
+    if (OUT8) {
+        uint32_t u[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            qv[i] = fminf(fmaxf(rintf(__fdiv_rn(f[i], qz.s)), -127.0f), 127.0f);
+            u[i] = __float_as_uint(m[i]);
+        const uint32_t lo = __byte_perm(__byte_perm(u[0], u[1], 0x0040), __byte_perm(u[2], u[3], 0x0040), 0x5410);
+        const uint32_t hi = __byte_perm(__byte_perm(u[4], u[5], 0x0040), __byte_perm(u[6], u[7], 0x0040), 0x5410);
+        *reinterpret_cast<uint2*>(q8 + off) = make_uint2(lo, hi);
     } else {
+        uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            qv[i] = 0.0f;
+        for (int i = 0; i < 4; ++i)
+            w[i] = __byte_perm(__float_as_uint(__fsub_rn(m[2 * i], kRoundMagic)),
+                               __float_as_uint(__fsub_rn(m[2 * i + 1], kRoundMagic)), 0x7632);
+        *reinterpret_cast<uint4*>(q16 + off) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
+// The codes of one vector (8 values) by the rule of `cd` (branching once per vector:
+// the rule is uniform over a row, or over the tensor), stored as int8 codes and/or bf16
+// codes at element offset `off`.
 template <bool OUT8, bool OUT16>
-__device__ __forceinline__ void store8(const float (&qv)[8], int8_t* q8, __nv_bfloat16* q16, int64_t off)
+__device__ __forceinline__ void code_store8(const Coder& cd, const float (&f)[8], int8_t* q8, __nv_bfloat16* q16,
+                                            int64_t off)
 {
-    if (OUT8) {
-        uint32_t lo = 0, hi = 0;
+    float m[8];
+    if (cd.kind == 1) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            lo |= ((uint32_t)__float2int_rn(qv[i]) & 0xFFu) << (8 * i);
-            hi |= ((uint32_t)__float2int_rn(qv[4 + i]) & 0xFFu) << (8 * i);
-        }
-        *reinterpret_cast<uint2*>(q8 + off) = make_uint2(lo, hi);
-    }
-    if (OUT16) {
-        uint32_t w[4];
+        for (int e = 0; e < 8; ++e)
+            m[e] = cd.magic1(f[e]);
+    } else if (cd.kind == 3) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 b = __floats2bfloat162_rn(qv[2 * i], qv[2 * i + 1]);
-            w[i] = *reinterpret_cast<uint32_t*>(&b);
-        }
-        *reinterpret_cast<uint4*>(q16 + off) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int e = 0; e < 8; ++e)
+            m[e] = cd.magic3(f[e]);
+    } else {
+        for (int e = 0; e < 8; ++e)
+            m[e] = cd.magic(f[e]);
     }
+    if (OUT8)
+        store_magic8<true>(m, q8, nullptr, off);
+    if (OUT16)
+        store_magic8<false>(m, nullptr, q16, off);
+}
+
+// bf16 bits -> fp32 (exact), two per 32-bit word, without conversion instructions.
+__device__ __forceinline__ void unpack8_bits(const uint4& v, float (&f)[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// 8 int8 weight codes (given as the two 32-bit halves of 8 bytes) -> 8 bf16 codes: byte
+// b ^ 0x80 is b + 128 as an unsigned byte; placed in the low mantissa of 2^23 and reduced
+// by 2^23 + 128 it is b as an exact float, whose upper half is its bf16.
+__device__ __forceinline__ uint4 widen8_bits(uint32_t lo, uint32_t hi)
+{
+    const uint32_t w[2] = {lo ^ 0x80808080u, hi ^ 0x80808080u};
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const uint32_t word = w[h >> 1];
+        const float a = __fsub_rn(__uint_as_float(0x4B000000u | ((word >> (16 * (h & 1))) & 0xFFu)), 8388736.0f);
+        const float b = __fsub_rn(__uint_as_float(0x4B000000u | ((word >> (16 * (h & 1) + 8)) & 0xFFu)), 8388736.0f);
+        o[h] = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ConvRot block transform of the 8 values a lane holds for one vector slot.  A
@@ -176,20 +258,8 @@ __device__ __forceinline__ void fwht_slot(float (&v)[8], int lane)
 // int8 -> bf16 (exact), 16 values per thread and vector.
 __device__ __forceinline__ void widen16(const uint4& v, uint4& lo, uint4& hi)
 {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float a = (float)(int8_t)((w[k] >> (16 * h)) & 0xFFu);
-            const float b = (float)(int8_t)((w[k] >> (16 * h + 8)) & 0xFFu);
-            __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
-            o[2 * k + h] = *reinterpret_cast<uint32_t*>(&p);
-        }
-    }
-    lo = make_uint4(o[0], o[1], o[2], o[3]);
-    hi = make_uint4(o[4], o[5], o[6], o[7]);
+    lo = widen8_bits(v.x, v.y);
+    hi = widen8_bits(v.z, v.w);
 }
 
 // This block's share of an int8 -> bf16 widening, called by every thread of the block.
@@ -278,7 +348,7 @@ __global__ void __launch_bounds__(THREADS) rows_kernel(const uint4* __restrict__
     if (ROT) {
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-            unpack8(raw[j], v[j]);
+            unpack8_bits(raw[j], v[j]);
             if (warp_first + (int64_t)TPR * j < nvec) {  // warp-uniform
                 fwht_slot(v[j], lane);
 #pragma unroll
@@ -299,23 +369,21 @@ __global__ void __launch_bounds__(THREADS) rows_kernel(const uint4* __restrict__
             amax = fmaxf(amax, red[g * WPR + i]);
     }
     if (live) {
-        const float s = __fdiv_rn(amax, 127.0f);
+        const float s = div127(amax);
         if (t == 0)
             xs[row] = s;
-        const Quantizer qz(s, ROT);
+        const Coder cd(s, ROT);
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int64_t idx = t + (int64_t)TPR * j;
             if (idx < nvec) {
-                float qv[8];
                 if (ROT) {
-                    quantize8(qz, v[j], qv);
+                    code_store8<OUT8, OUT16>(cd, v[j], q8, q16, row * K + idx * 8);
                 } else {
                     float f[8];
-                    unpack8(raw[j], f);
-                    quantize8(qz, f, qv);
+                    unpack8_bits(raw[j], f);
+                    code_store8<OUT8, OUT16>(cd, f, q8, q16, row * K + idx * 8);
                 }
-                store8<OUT8, OUT16>(qv, q8, q16, row * K + idx * 8);
             }
         }
     }
@@ -336,7 +404,7 @@ __device__ __forceinline__ void stream_row(const uint4* __restrict__ x, int64_t 
         const int64_t idx = base + lane;
         const uint4 r = (idx < nvec) ? xr[idx] : make_uint4(0, 0, 0, 0);
         float f[8];
-        unpack8(r, f);
+        unpack8_bits(r, f);
         if (ROT)
             fwht_slot(f, lane);
         if (idx < nvec) {
@@ -346,21 +414,19 @@ __device__ __forceinline__ void stream_row(const uint4* __restrict__ x, int64_t 
         }
     }
     amax = warp_max(amax);
-    const float s = __fdiv_rn(amax, 127.0f);
+    const float s = div127(amax);
     if (lane == 0)
         xs[row] = s;
-    const Quantizer qz(s, ROT);
+    const Coder cd(s, ROT);
     for (int64_t base = 0; base < nvec; base += 32) {
         const int64_t idx = base + lane;
         const uint4 r = (idx < nvec) ? ld_stream(xr + idx) : make_uint4(0, 0, 0, 0);
-        float f[8], qv[8];
-        unpack8(r, f);
+        float f[8];
+        unpack8_bits(r, f);
         if (ROT)
             fwht_slot(f, lane);
-        if (idx < nvec) {
-            quantize8(qz, f, qv);
-            store8<OUT8, OUT16>(qv, q8, q16, row * K + idx * 8);
-        }
+        if (idx < nvec)
+            code_store8<OUT8, OUT16>(cd, f, q8, q16, row * K + idx * 8);
     }
 }
 
@@ -439,18 +505,15 @@ __global__ void __launch_bounds__(THREADS) weight_rot_kernel(const float4* __res
     }
     if (!live)
         return;
-    const float s = __fdiv_rn(amax, 127.0f);
+    const float s = div127(amax);
     if (t == 0)
         ws[row] = s;
-    const Quantizer qz(s, true);
+    const Coder cd(s, true);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int64_t idx = t + (int64_t)TPR * j;
-        if (idx < nvec) {
-            float qv[8];
-            quantize8(qz, v[j], qv);
-            store8<true, false>(qv, w, nullptr, row * K + idx * 8);
-        }
+        if (idx < nvec)
+            code_store8<true, false>(cd, v[j], w, nullptr, row * K + idx * 8);
     }
 }
 
@@ -480,19 +543,17 @@ __global__ void __launch_bounds__(THREADS) weight_rot_stream_kernel(const float4
         }
     }
     amax = warp_max(amax);
-    const float s = __fdiv_rn(amax, 127.0f);
+    const float s = div127(amax);
     if (lane == 0)
         ws[row] = s;
-    const Quantizer qz(s, true);
+    const Coder cd(s, true);
     for (int64_t base = 0; base < nvec; base += 32) {
         const int64_t idx = base + lane;
-        float f[8], qv[8];
+        float f[8];
         load8_f32(wr, idx, idx < nvec, f);
         fwht_slot(f, lane);
-        if (idx < nvec) {
-            quantize8(qz, f, qv);
-            store8<true, false>(qv, w, nullptr, row * K + idx * 8);
-        }
+        if (idx < nvec)
+            code_store8<true, false>(cd, f, w, nullptr, row * K + idx * 8);
     }
 }
 
@@ -557,10 +618,10 @@ __global__ void __launch_bounds__(256) quant_flat_kernel(const uint4* __restrict
             s_amax = m;
     }
     __syncthreads();
-    const float s = __fdiv_rn(s_amax, 127.0f);
+    const float s = div127(s_amax);
     if (blockIdx.x == 0 && threadIdx.x == 0)
         xs[0] = s;
-    const Quantizer qz(s, false);
+    const Coder cd(s, false);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec; base += UNROLL * stride) {
         uint4 v[UNROLL];
@@ -573,10 +634,9 @@ __global__ void __launch_bounds__(256) quant_flat_kernel(const uint4* __restrict
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t i = base + u * stride;
             if (i < nvec) {
-                float f[8], qv[8];
-                unpack8(v[u], f);
-                quantize8(qz, f, qv);
-                store8<OUT8, OUT16>(qv, q8, q16, i * 8);
+                float f[8];
+                unpack8_bits(v[u], f);
+                code_store8<OUT8, OUT16>(cd, f, q8, q16, i * 8);
             }
         }
     }
@@ -726,7 +786,7 @@ __global__ void __launch_bounds__(TPB) tensorwise_prep_kernel(
     float g = 0.0f;
     for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
         g = fmaxf(g, red[i]);
-    const float sc = gave_up ? __int_as_float(0x7FFFFFFF) : __fdiv_rn(g, 127.0f);
+    const float sc = gave_up ? __int_as_float(0x7FFFFFFF) : div127(g);
     if (threadIdx.x == 0) {
         if (gave_up) {
             st_relaxed_u64(poison, epoch);
@@ -737,7 +797,7 @@ __global__ void __launch_bounds__(TPB) tensorwise_prep_kernel(
         }
     }
     // 4. quantize this block's slice
-    const Quantizer qz(sc, false);
+    const Coder cd(sc, false);
     slot = 0;
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < nvec;
          base += UNROLL * stride, slot += UNROLL) {
@@ -754,10 +814,9 @@ __global__ void __launch_bounds__(TPB) tensorwise_prep_kernel(
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t i = base + u * stride;
             if (i < nvec) {
-                float f[8], qv[8];
-                unpack8(v[u], f);
-                quantize8(qz, f, qv);
-                store8<false, true>(qv, nullptr, q16, i * 8);
+                float f[8];
+                unpack8_bits(v[u], f);
+                code_store8<false, true>(cd, f, nullptr, q16, i * 8);
             }
         }
     }
@@ -787,7 +846,7 @@ __global__ void __launch_bounds__(256) rotate_bf16_kernel(const uint4* __restric
         // (lanes 16-31 then idle: their shuffle partners stay within lanes 16-31)
         const uint4 raw = i < nvec ? ld_stream(x + i) : make_uint4(0, 0, 0, 0);
         float v[8];
-        unpack8(raw, v);
+        unpack8_bits(raw, v);
         fwht_slot(v, lane);
         if (i < nvec) {
             uint32_t o[4];
@@ -963,7 +1022,6 @@ cudaError_t launch_widen_int8(const int8_t* src, void* dst, int64_t n, const Dev
 cudaError_t launch_prep_rows(const void* x, int64_t M, int64_t K, bool rotate, void* q16, float* x_scale,
                              const int8_t* w8, int64_t w_n, void* w16, const DeviceInfo& dev, cudaStream_t s)
 {
-    (void)dev;
     if (M == 0)
         return launch_widen_int8(w8, w16, w_n, dev, s);
     return rows_dispatch<false, true>(x, M, K, rotate, nullptr, q16, x_scale, w8, w_n, w16, s);

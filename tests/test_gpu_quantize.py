@@ -132,3 +132,17 @@ def test_convrot_weight_preparation_rejects_unaligned_k():
     with pytest.raises(ck.CkError) as e:
         ck.ck_convrot_prepare_weight(W)
     assert "128" in str(e.value)
+
+
+def test_every_bf16_row_maximum():
+    """x_scale = fl(max|x| / 127) for every finite non-negative bf16 row maximum (32640
+    of them, subnormals and zero included), and the codes of a row holding its maximum,
+    its negative, a third of it and zeros: bit-exact with the oracle's IEEE division."""
+    amax = np.arange(0, 0x7F80, dtype=np.uint16)
+    K = 16
+    xb = np.zeros((amax.size, K), np.uint16)
+    xb[:, 0] = amax
+    xb[:, 1] = amax | 0x8000
+    third = (torch.from_numpy(amax.view(np.int16)).view(torch.bfloat16).float() / 3).to(torch.bfloat16)
+    xb[:, 2] = bits(third)
+    check_rowwise(from_bits(xb), rotate=False)
