@@ -40,7 +40,7 @@
  *   - Device: compute capability 10.3 (GB300) only, else CK_ERR_UNSUPPORTED_DEVICE.
  *     There is no fallback path of any kind.
  *   - CUDA graphs: every entry point except ck_quantize_int8_tensorwise_noalloc (whose
- *     capture is not covered here) may be captured (cudaStreamBeginCapture) and the
+ *     capture is not covered here) and ck_int8_linear_host (refused) may be captured (cudaStreamBeginCapture) and the
  *     graph replayed with new data in the same buffers; the results equal uncaptured
  *     calls.  Make one uncaptured call per device first (it sets kernel attributes and
  *     looks up the library's device symbols).  Under capture, ck_int8_linear in
@@ -169,6 +169,30 @@ int ck_int8_linear_workspace_views(int64_t M, int64_t N, int64_t K, int mode, si
 int ck_int8_linear(const void *x, const int8_t *w, const float *w_scale, const void *bias, const void *residual,
                    void *y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype, void *workspace,
                    size_t workspace_bytes, void *stream);
+
+/* The same layer with the activation read from and the output written to HOST memory
+ * (issue #136's int8_linear(x, w, ws, out_dtype) called on host tensors; the weight,
+ * its scales and the bias stay resident on the device):
+ *   x_host:  bf16 [M,K] host memory, read.  y_host: [M,N] of out_dtype host memory,
+ *            written.  Page-locked (pinned) host memory lets the copies overlap the
+ *            kernels; pageable memory gives the same result with the copies serialized.
+ *   w, w_scale, bias, mode, out_dtype: as for ck_int8_linear (device memory); no residual.
+ *   slab_rows: rows per pipeline slab (0: about 256 MB of output per slab).  The call
+ *            cuts M into slabs and overlaps, on two internal copy streams of the current
+ *            context (made on its first call there) and the caller's stream, the copy of
+ *            slab i+1 to the device, the kernels of slab i and the copy of slab i-1 back.
+ *            CK_TENSORWISE copies all of x first (its one scale needs every value).
+ *   workspace: ck_int8_linear_host_workspace_size(M, N, K, mode, out_dtype, slab_rows)
+ *            bytes of device memory (two activation and two output slab buffers, the
+ *            codes, the widened weight).
+ * y_host is complete once the caller's stream has completed past this call (the stream
+ * waits for the last copy).  The results equal ck_int8_linear's bit for bit.  Cannot be
+ * captured into a CUDA graph (CK_ERR_INVALID_ARG). */
+size_t ck_int8_linear_host_workspace_size(int64_t M, int64_t N, int64_t K, int mode, int out_dtype,
+                                          int64_t slab_rows);
+int ck_int8_linear_host(const void *x_host, const int8_t *w, const float *w_scale, const void *bias, void *y_host,
+                        int64_t M, int64_t N, int64_t K, int mode, int out_dtype, int64_t slab_rows, void *workspace,
+                        size_t workspace_bytes, void *stream);
 
 /* ConvRot weight preparation (issue #278, "Suggested fix": the stored weight is
  * W_rot = W @ H^T; since H is symmetric, row n of it is row n of W times H), quantized

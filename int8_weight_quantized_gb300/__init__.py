@@ -52,6 +52,8 @@ def load_library(path=None):
         "ck_int8_linear_workspace_views": ([I64, I64, I64, I, ctypes.POINTER(SZ), ctypes.POINTER(SZ)], I),
         "ck_int8_linear": ([P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_convrot_prepare_weight": ([P, I64, I64, P, P, P], I),
+        "ck_int8_linear_host_workspace_size": ([I64, I64, I64, I, I, I64], SZ),
+        "ck_int8_linear_host": ([P, P, P, P, P, I64, I64, I64, I, I, I64, P, SZ, P], I),
         "ck_int8_gemm_workspace_size": ([I64, I64, I64], SZ),
         "ck_w8a16_linear_workspace_size": ([I64, I64, I64, I], SZ),
         "ck_w8a16_linear": ([P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
@@ -208,6 +210,32 @@ def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stre
     _residual(residual, out_dtype, M, N)
     _check(L.ck_int8_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(residual), _ptr(y), M, N, K, int(mode),
                             code, _ptr(ws), ws.numel(), _stream(stream)))
+    return y
+
+
+def ck_int8_linear_host(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stream=None,
+                        out_dtype=torch.bfloat16, slab_rows=0):
+    """The layer on a HOST activation x bf16 [M,K] (pinned for overlapped copies) into a
+    host output y [M,N] of out_dtype; w, w_scale, bias on the device.  The copies and the
+    kernels are pipelined over row slabs; y is complete when `stream` has completed."""
+    code = _out_code(out_dtype)
+    M, K = x.shape
+    N = w.shape[0]
+    if x.dtype != torch.bfloat16 or x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 host tensor")
+    _req(w, torch.int8, (N, K), "w")
+    _req(w_scale, torch.float32, (1,) if mode == TENSORWISE else (N,), "w_scale")
+    if bias is not None:
+        _req(bias, torch.bfloat16, (N,), "bias")
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, pin_memory=x.is_pinned())
+    if y.dtype != out_dtype or tuple(y.shape) != (M, N) or y.is_cuda or not y.is_contiguous():
+        raise ValueError("y must be a contiguous host tensor of shape %s and type %s" % ((M, N), out_dtype))
+    L = load_library()
+    need = L.ck_int8_linear_host_workspace_size(M, N, K, int(mode), code, int(slab_rows))
+    ws = workspace(need, w.device) if ws is None else ws
+    _check(L.ck_int8_linear_host(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, int(mode), code,
+                                 int(slab_rows), _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 

@@ -772,6 +772,234 @@ int ck_selftest_wait_timeout(uint64_t timeout_ns, void* stream)
 }  // extern "C"
 
 // ---------------------------------------------------------------------------------
+// The layer with the activation and the output in host memory.
+//
+// The rows of the layer are independent (per-row and ConvRot scales are per row; the
+// tensorwise scale needs all of x once, then the GEMM rows are again independent), so
+// the call cuts M into slabs and overlaps, on three streams, the copy of slab i+1's
+// activation into the device, the preparation and GEMM of slab i, and the copy of slab
+// i-1's output back to the host.  Two device buffers alternate for the incoming
+// activation and two for the outgoing output; events order each buffer's reuse.  The
+// copies run on two internal streams per context (created on the first call there),
+// the kernels on the caller's stream, which at the end waits for the last copy back: when
+// the caller's stream has finished, y is complete in host memory.
+namespace ck {
+namespace {
+
+struct HostLayout {
+    int64_t R;          // rows per slab
+    size_t x_slab, y_slab;
+    size_t off_x[2], off_y[2], off_a16, off_xs, off_scratch, off_b16, off_tail, total;
+};
+
+int64_t host_slab_rows(int64_t M, int64_t N, int out_dtype, int64_t slab_rows)
+{
+    if (slab_rows > 0)
+        return std::min<int64_t>(slab_rows, std::max<int64_t>(M, 1));
+    // about 256 MB of output per slab, in whole 256-row tile pairs
+    const int64_t osize = out_dtype == CK_OUT_F32 ? 4 : 2;
+    int64_t r = ((int64_t)256 << 20) / std::max<int64_t>(1, N * osize);
+    r = std::max<int64_t>(256, r / 256 * 256);
+    return std::min<int64_t>(r, std::max<int64_t>(M, 1));
+}
+
+HostLayout host_layout(int64_t M, int64_t N, int64_t K, int mode, int out_dtype, int64_t slab_rows)
+{
+    HostLayout L;
+    L.R = host_slab_rows(M, N, out_dtype, slab_rows);
+    const int64_t osize = out_dtype == CK_OUT_F32 ? 4 : 2;
+    const bool tw = mode == CK_TENSORWISE;
+    // tensorwise keeps all of x and its codes on the device (one scale for the tensor)
+    L.x_slab = align_up((size_t)(tw ? M : L.R) * K * 2);
+    L.y_slab = align_up((size_t)L.R * N * osize);
+    size_t o = 0;
+    L.off_x[0] = o;
+    o += L.x_slab;
+    L.off_x[1] = tw ? L.off_x[0] : o;
+    if (!tw)
+        o += L.x_slab;
+    L.off_a16 = o;
+    o += L.x_slab;
+    L.off_xs = o;
+    o += align_up(sizeof(float) * (size_t)(tw ? 1 : L.R));
+    L.off_scratch = o;
+    o += align_up(prep_tensorwise_scratch_bytes(kMaxPartialsForLayout));
+    L.off_b16 = o;
+    o += align_up((size_t)N * K * 2);
+    L.off_y[0] = o;
+    o += L.y_slab;
+    L.off_y[1] = o;
+    o += L.y_slab;
+    L.off_tail = o;
+    o += align_up(gemm_tail_bytes(L.R, N));
+    L.total = o;
+    return L;
+}
+
+// The two copy streams of the current context and the events that order the buffers.
+struct HostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start, done, x_ready[2], x_free[2], y_ready[2], y_free[2];
+    std::mutex* mu = nullptr;
+};
+
+cudaError_t host_pipe(HostPipe* out)
+{
+    static ContextCache<HostPipe> cache;
+    return cache.get(out, [](HostPipe* p) {
+        cudaError_t e = cudaStreamCreateWithFlags(&p->in, cudaStreamNonBlocking);
+        if (e == cudaSuccess)
+            e = cudaStreamCreateWithFlags(&p->out, cudaStreamNonBlocking);
+        cudaEvent_t* evs[] = {&p->start, &p->done, &p->x_ready[0], &p->x_ready[1], &p->x_free[0],
+                              &p->x_free[1],  &p->y_ready[0], &p->y_ready[1], &p->y_free[0], &p->y_free[1]};
+        for (cudaEvent_t* ev : evs)
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        p->mu = new std::mutex();
+        return e;
+    });
+}
+
+}  // namespace
+}  // namespace ck
+
+extern "C" size_t ck_int8_linear_host_workspace_size(int64_t M, int64_t N, int64_t K, int mode, int out_dtype,
+                                                      int64_t slab_rows)
+{
+    if (M < 0 || N < 0 || K < 0 || slab_rows < 0)
+        return 0;
+    return host_layout(M, N, K, mode, out_dtype, slab_rows).total;
+}
+
+extern "C" int ck_int8_linear_host(const void* x_host, const int8_t* w, const float* w_scale, const void* bias,
+                                   void* y_host, int64_t M, int64_t N, int64_t K, int mode, int out_dtype,
+                                   int64_t slab_rows, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (mode != CK_TENSORWISE && mode != CK_PER_ROW && mode != CK_CONVROT)
+        return fail(CK_ERR_INVALID_ARG, "mode must be 0 (tensorwise), 1 (per-row) or 2 (ConvRot), got %d", mode);
+    if (!valid_out_dtype(out_dtype))
+        return fail(CK_ERR_INVALID_ARG, "out_dtype must be 0 (bf16), 1 (fp16) or 2 (fp32), got %d", out_dtype);
+    int st = check_gemm_shape(M, N, K);
+    if (st != CK_OK)
+        return st;
+    if (mode == CK_CONVROT && K % 128 != 0)
+        return fail(CK_ERR_INVALID_ARG, "ConvRot needs K % 128 == 0 (got %lld)", (long long)K);
+    if (slab_rows < 0)
+        return fail(CK_ERR_INVALID_ARG, "slab_rows must be >= 0 (0: chosen by the library)");
+    if (M == 0)
+        return CK_OK;
+    CK_REQUIRE_PTR(x_host);
+    CK_REQUIRE_PTR(w);
+    CK_REQUIRE_PTR(w_scale);
+    CK_REQUIRE_PTR(y_host);
+    CK_REQUIRE_PTR(workspace);
+    if (bias != nullptr && !aligned16(bias))
+        return fail(CK_ERR_INVALID_ARG, "bias must be 16-byte aligned");
+    const HostLayout L = host_layout(M, N, K, mode, out_dtype, slab_rows);
+    if (workspace_bytes < L.total)
+        return fail(CK_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, L.total);
+    DeviceInfo dev;
+    if ((st = check_device(&dev)) != CK_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (stream_capturing(s))
+        return fail(CK_ERR_INVALID_ARG, "ck_int8_linear_host cannot be captured into a CUDA graph");
+    HostPipe hp;
+    cudaError_t e = host_pipe(&hp);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "creating the copy streams");
+    std::lock_guard<std::mutex> lock(*hp.mu);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const uint8_t* xh = static_cast<const uint8_t*>(x_host);
+    uint8_t* yh = static_cast<uint8_t*>(y_host);
+    const bool tw = mode == CK_TENSORWISE;
+    const int64_t osize = out_dtype == CK_OUT_F32 ? 4 : 2;
+    const int64_t slabs = (M + L.R - 1) / L.R;
+    float* xs = reinterpret_cast<float*>(ws + L.off_xs);
+    void* a16 = ws + L.off_a16;
+    void* b16 = ws + L.off_b16;
+    if (log_enabled())
+        log_shape("int8_linear_host", M, N, K, mode,
+                  std::to_string(slabs) + " slabs of " + std::to_string(L.R) + " rows, copies on two streams");
+#define CK_TRY(expr, what)                  \
+    do {                                    \
+        if ((e = (expr)) != cudaSuccess)    \
+            return cuda_fail(e, what);      \
+    } while (0)
+    // the copy streams start after the work already on the caller's stream
+    CK_TRY(cudaEventRecord(hp.start, s), "ck_int8_linear_host event");
+    CK_TRY(cudaStreamWaitEvent(hp.in, hp.start, 0), "ck_int8_linear_host wait");
+    CK_TRY(cudaStreamWaitEvent(hp.out, hp.start, 0), "ck_int8_linear_host wait");
+    if (tw) {
+        // all of x, then one preparation: the tensor's scale needs every value
+        CK_TRY(cudaMemcpyAsync(ws + L.off_x[0], xh, (size_t)M * K * 2, cudaMemcpyHostToDevice, hp.in),
+               "copying x to the device");
+        CK_TRY(cudaEventRecord(hp.x_ready[0], hp.in), "ck_int8_linear_host event");
+        CK_TRY(cudaStreamWaitEvent(s, hp.x_ready[0], 0), "ck_int8_linear_host wait");
+        {
+            ProfScope ps(kProfQuantize, 1, s);
+            CK_TRY(launch_prep_tensorwise(ws + L.off_x[0], M, K, a16, xs, ws + L.off_scratch, kMaxPartialsForLayout, w,
+                                          N * K, b16, dev, s),
+                   "ck_int8_linear_host preparation launch");
+        }
+    }
+    for (int64_t i = 0; i < slabs; ++i) {
+        const int b = (int)(i & 1);
+        const int64_t r0 = i * L.R;
+        const int64_t rows = std::min<int64_t>(L.R, M - r0);
+        if (!tw) {
+            // activation slab in (after the preparation that last read this buffer)
+            CK_TRY(cudaStreamWaitEvent(hp.in, hp.x_free[b], 0), "ck_int8_linear_host wait");
+            CK_TRY(cudaMemcpyAsync(ws + L.off_x[b], xh + r0 * K * 2, (size_t)rows * K * 2, cudaMemcpyHostToDevice,
+                                   hp.in),
+                   "copying an x slab to the device");
+            CK_TRY(cudaEventRecord(hp.x_ready[b], hp.in), "ck_int8_linear_host event");
+            CK_TRY(cudaStreamWaitEvent(s, hp.x_ready[b], 0), "ck_int8_linear_host wait");
+            ProfScope ps(kProfQuantize, 1, s);
+            // the weight is widened once, by the first slab's launch
+            CK_TRY(launch_prep_rows(ws + L.off_x[b], rows, K, mode == CK_CONVROT, a16, xs, i == 0 ? w : nullptr,
+                                    N * K, b16, dev, s),
+                   "ck_int8_linear_host preparation launch");
+            CK_TRY(cudaEventRecord(hp.x_free[b], s), "ck_int8_linear_host event");
+        }
+        // the GEMM of the slab into an output buffer the previous copy back has released
+        CK_TRY(cudaStreamWaitEvent(s, hp.y_free[b], 0), "ck_int8_linear_host wait");
+        GemmProblem p;
+        p.a = static_cast<uint8_t*>(a16) + (tw ? r0 * K * 2 : 0);
+        p.b = b16;
+        p.M = rows;
+        p.N = N;
+        p.K = K;
+        p.x_scale = xs;
+        p.w_scale = w_scale;
+        p.bias = bias;
+        p.scalar_scales = tw;
+        p.y = ws + L.off_y[b];
+        p.out_dtype = out_dtype;
+        p.tail = ws + L.off_tail;
+        std::string why;
+        {
+            ProfScope ps(kProfGemm, 1, s);
+            e = launch_gemm(p, dev, s, &why);
+        }
+        if (e != cudaSuccess)
+            return why.empty() ? cuda_fail(e, "ck_int8_linear_host GEMM launch") : fail(CK_ERR_CUDA, "%s", why.c_str());
+        CK_TRY(cudaEventRecord(hp.y_ready[b], s), "ck_int8_linear_host event");
+        // ... and the slab's output back to the host
+        CK_TRY(cudaStreamWaitEvent(hp.out, hp.y_ready[b], 0), "ck_int8_linear_host wait");
+        CK_TRY(cudaMemcpyAsync(yh + r0 * N * osize, ws + L.off_y[b], (size_t)rows * N * osize, cudaMemcpyDeviceToHost,
+                               hp.out),
+               "copying a y slab to the host");
+        CK_TRY(cudaEventRecord(hp.y_free[b], hp.out), "ck_int8_linear_host event");
+    }
+    // the caller's stream completes only after the last copy back
+    CK_TRY(cudaEventRecord(hp.done, hp.out), "ck_int8_linear_host event");
+    CK_TRY(cudaStreamWaitEvent(s, hp.done, 0), "ck_int8_linear_host wait");
+#undef CK_TRY
+    return CK_OK;
+}
+
+// ---------------------------------------------------------------------------------
 // Tensorwise quantize without any allocation.
 //
 // Some callers cannot allocate device memory at all.  A real-time inference loop may

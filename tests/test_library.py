@@ -155,3 +155,21 @@ def test_workspace_views(lib):
     sz = ctypes.c_size_t()
     assert lib.ck_int8_linear_workspace_views(16, 8, 16, 7, ctypes.byref(sz), ctypes.byref(sz)) == ck.CK_ERR_INVALID_ARG
     assert lib.ck_int8_linear_workspace_views(16, 8, 16, 1, None, ctypes.byref(sz)) == ck.CK_ERR_INVALID_ARG
+
+
+def test_host_layer_arguments(lib):
+    """The host-memory layer: workspace sizes grow with the slab, bad arguments are
+    rejected before any device work."""
+    import ctypes
+    import int8_weight_quantized_gb300 as ck
+    a = lib.ck_int8_linear_host_workspace_size(10000, 4096, 2048, ck.PER_ROW, 0, 512)
+    b = lib.ck_int8_linear_host_workspace_size(10000, 4096, 2048, ck.PER_ROW, 0, 1024)
+    assert 2 * 512 * 4096 * 2 <= a < b
+    # tensorwise keeps all of x on the device
+    assert lib.ck_int8_linear_host_workspace_size(10000, 4096, 2048, ck.TENSORWISE, 0, 512) > a
+    P = ctypes.c_void_p
+    ptr = P(4096)
+    st = lib.ck_int8_linear_host(ptr, ptr, ptr, None, ptr, 64, 64, 64, ck.PER_ROW, 0, -1, ptr, 1 << 40, None)
+    assert st == ck.CK_ERR_INVALID_ARG and "slab_rows" in ck.ck_last_error()
+    st = lib.ck_int8_linear_host(ptr, ptr, ptr, None, ptr, 64, 64, 60, ck.PER_ROW, 0, 0, ptr, 1 << 40, None)
+    assert st == ck.CK_ERR_INVALID_ARG
