@@ -240,13 +240,15 @@ __device__ __forceinline__ void fwht_slot(float (&v)[8], int lane)
             }
         }
     }
+    // across lanes: the lower lane of a pair keeps v + p, the upper one p - v; both are
+    // one correctly rounded fma(+-1, v, p) (the product by +-1 is exact)
 #pragma unroll
     for (int hl = 1; hl < 16; hl <<= 1) {
-        const bool upper = (lane & hl) != 0;
+        const float sgn = (lane & hl) ? -1.0f : 1.0f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float p = __shfl_xor_sync(0xffffffffu, v[e], hl);
-            v[e] = upper ? __fsub_rn(p, v[e]) : __fadd_rn(v[e], p);
+            v[e] = __fmaf_rn(sgn, v[e], p);
         }
     }
     const float c128 = 0.088388346f;  // fp32(1/sqrt(128)) = 0x3DB504F3

@@ -15,7 +15,9 @@ the library's own per-launch choice.
 
 Only the GEMM kernel is timed (CUDA events around it, via ck_profile_begin); L2 is
 flushed before every timed launch (a 512 MiB write, then a 256 MiB read so no dirty
-lines are left to write back).  Forcing a configuration uses the library's A/B
+lines are left to write back).  The configurations of a shape are timed in rounds (one
+launch of each per round) and the median over the rounds is kept, so clock drift under
+the power cap does not favour the configurations timed first.  Forcing a configuration uses the library's A/B
 overrides CK_GEMM_PAIR / CK_GEMM_BN / CK_GEMM_SPLIT, set in this process's environment.
 """
 import argparse
@@ -58,25 +60,24 @@ def flush_l2(flush):
     torch.sum(flush[1], dim=0, out=flush[2])
 
 
-def time_config(args, flush, pair, bn, reps, split=None, warmup=2):
-    """Median GEMM milliseconds with the configuration forced (None = the library's pick;
-    split=1 turns the K-split of the last partial wave off)."""
+def _launch_ms(args, flush, cfg):
+    """One flushed, event-bracketed GEMM launch with configuration cfg = (pair, bn, split)
+    forced (pair None = the library's own pick; split 1 = no K-split)."""
+    pair, bn, split = cfg
     _set_override(None if pair is None else (1 if pair else 0), bn, split)
     try:
-        for _ in range(warmup):
-            ck_int8_gemm_dequant(*args)
-        times = []
-        for _ in range(reps):
-            flush_l2(flush)
-            ck_profile_begin(with_events=True)
-            ck_int8_gemm_dequant(*args)
-            times.append(ck_profile_end()["gemm"][0])
-        return statistics.median(times)
+        flush_l2(flush)
+        ck_profile_begin(with_events=True)
+        ck_int8_gemm_dequant(*args)
+        return ck_profile_end()["gemm"][0]
     finally:
         _set_override(None, None)
 
 
 def sweep_shape(M, N, K, reps, flush, seed=7):
+    """Every configuration of one shape, timed in rounds: each round launches every
+    configuration once, so a drift of the clocks (the power cap of long launches) hits all
+    of them alike; the median over the rounds is reported."""
     dev = "cuda"
     q = synthetic.int8_uniform((M, K), seed, device=dev)
     w = synthetic.int8_uniform((N, K), seed + 1, device=dev)
@@ -85,18 +86,27 @@ def sweep_shape(M, N, K, reps, flush, seed=7):
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     args = (q, xs, w, ws, None, False, y)
     pick_bn, pick_pair, resident, pick_split = ck_gemm_tile_config(M, N, K)
-    configs = {}
+    cfgs = {}
     pairs = [True, False] if (M + 127) // 128 >= 2 else [False]
     for pair in pairs:
         for bn in WIDTHS:
             name = "%s/%d" % ("pair" if pair else "single", bn)
-            configs[name] = time_config(args, flush, pair, bn, reps, split=1)
+            cfgs[name] = (pair, bn, 1)
             _set_override(1 if pair else 0, bn)
             split = ck_gemm_tile_config(M, N, K)[3]
             _set_override(None, None)
             if split > 1:
-                configs["%s/split%d" % (name, split)] = time_config(args, flush, pair, bn, reps)
-    picked_ms = time_config(args, flush, None, None, reps)
+                cfgs["%s/split%d" % (name, split)] = (pair, bn, None)
+    cfgs["picked"] = (None, None, None)
+    for cfg in cfgs.values():  # warm-up: every instance loaded, attributes set
+        for _ in range(2):
+            _launch_ms(args, flush, cfg)
+    samples = {name: [] for name in cfgs}
+    for _ in range(reps):
+        for name, cfg in cfgs.items():
+            samples[name].append(_launch_ms(args, flush, cfg))
+    configs = {name: statistics.median(v) for name, v in samples.items() if name != "picked"}
+    picked_ms = statistics.median(samples["picked"])
     best = min(configs, key=configs.get)
     flops = 2.0 * M * N * K
     del q, w, xs, ws, y
