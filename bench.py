@@ -282,8 +282,13 @@ def run_ours(args, spec):
     b = None if case.bias is None else case.bias.to(dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     w8a16 = args.path == "w8a16"
+    codes = None
     if w8a16:
         work = ck.workspace(ck.load_library().ck_w8a16_linear_workspace_size(M, N, K, mode), dev)
+    elif args.weight_codes:
+        # the weight's bf16 codes, prepared once per layer (outside the steps)
+        codes = ck.ck_int8_weight_codes(w)
+        work = ck.workspace(ck.load_library().ck_int8_linear_codes_workspace_size(M, N, K, mode), dev)
     else:
         work = ck.workspace(ck.ck_int8_linear_workspace_size(M, N, K, mode), dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -299,6 +304,8 @@ def run_ours(args, spec):
     def step():
         if w8a16:
             ck.ck_w8a16_linear(x, w, ws_, b, mode=mode, y=y, ws=work)
+        elif codes is not None:
+            ck.ck_int8_linear_codes(x, codes, ws_, b, mode=mode, y=y, ws=work)
         else:
             ck.ck_int8_linear(x, w, ws_, b, mode=mode, y=y, ws=work)
 
@@ -377,7 +384,8 @@ def run_ours(args, spec):
         prep_moved = N * K + 2 * N * K + prep_alg
     else:
         prep_alg = (5 * M * K + 4) if mode == synthetic.TENSORWISE else (3 * M * K + 4 * M)
-        prep_moved = 2 * M * K + 2 * M * K + N * K + 2 * N * K + (4 if mode == synthetic.TENSORWISE else 4 * M)
+        prep_moved = 2 * M * K + 2 * M * K + (0 if codes is not None else N * K + 2 * N * K) + \
+            (4 if mode == synthetic.TENSORWISE else 4 * M)
     p_step = max(p_ms, 1e-9) / kt_steps
     roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
                 "frac": achieved / bf16_peak, "traffic": traffic,
@@ -433,8 +441,10 @@ def run_ours(args, spec):
     line = {"metric": METRICS[args.path], "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int8" if not w8a16 else "bf16", "data": "synthetic",
-            "config": workload_config(spec, "flushed between steps (%d MiB write, then %d MiB read); inputs %s L2" % (
+            "config": dict(workload_config(spec, "flushed between steps (%d MiB write, then %d MiB read); inputs %s L2" % (
                 FLUSH_BYTES >> 20, CLEAN_BYTES >> 20, "larger than" if M * K * 2 > L2_BYTES else "smaller than")),
+                           **({"weight": "bf16 codes prepared once per layer (ck_int8_linear_codes)"} if codes is not None
+                              else {})),
             "roofline": roofline, "kernels": kernels, "e2e": e2e, "clocks": clocks,
             "gpu_launches": int(sum(n for _, n in counts.values())), "timed_wall_s": wall}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -494,6 +504,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weight-codes", action="store_true",
+                    help="run the INT8 layer on the weight's bf16 codes prepared once (ck_int8_linear_codes) "
+                         "instead of widening the int8 weight in every step")
     ap.add_argument("--path", choices=sorted(METRICS), default="int8",
                     help="int8: the INT8 layer (the headline); w8a16: its 16-bit-activation path")
     args = ap.parse_args(argv)

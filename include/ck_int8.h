@@ -170,6 +170,21 @@ int ck_int8_linear(const void *x, const int8_t *w, const float *w_scale, const v
                    void *y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype, void *workspace,
                    size_t workspace_bytes, void *stream);
 
+/* The layer with the weight's GEMM operand prepared once, for callers that run a layer
+ * many times and can hold 2 B per weight on the device: the int8 weight (issue #136's w,
+ * int8 [N,K]) widened to its bf16 codes (every value an integer in [-127, 127], exact in
+ * bf16), which ck_int8_linear would otherwise redo in every call's preparation launch.
+ *   ck_int8_weight_codes: w int8 [N,K] device (read) -> w_codes bf16 [N,K] device
+ *     (written; caller-owned, N*K*2 bytes).  K % 16 == 0.
+ *   ck_int8_linear_codes: exactly ck_int8_linear (same arguments, same results bit for
+ *     bit) with w_codes in place of w; its workspace,
+ *     ck_int8_linear_codes_workspace_size(M, N, K, mode) bytes, holds no widened weight. */
+int ck_int8_weight_codes(const int8_t *w, int64_t N, int64_t K, void *w_codes, void *stream);
+size_t ck_int8_linear_codes_workspace_size(int64_t M, int64_t N, int64_t K, int mode);
+int ck_int8_linear_codes(const void *x, const void *w_codes, const float *w_scale, const void *bias,
+                         const void *residual, void *y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
 /* The same layer with the activation read from and the output written to HOST memory
  * (issue #136's int8_linear(x, w, ws, out_dtype) called on host tensors; the weight,
  * its scales and the bias stay resident on the device):

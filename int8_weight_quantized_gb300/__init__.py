@@ -52,6 +52,9 @@ def load_library(path=None):
         "ck_int8_linear_workspace_views": ([I64, I64, I64, I, ctypes.POINTER(SZ), ctypes.POINTER(SZ)], I),
         "ck_int8_linear": ([P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_convrot_prepare_weight": ([P, I64, I64, P, P, P], I),
+        "ck_int8_weight_codes": ([P, I64, I64, P, P], I),
+        "ck_int8_linear_codes_workspace_size": ([I64, I64, I64, I], SZ),
+        "ck_int8_linear_codes": ([P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P], I),
         "ck_int8_linear_host_workspace_size": ([I64, I64, I64, I, I, I64], SZ),
         "ck_int8_linear_host": ([P, P, P, P, P, I64, I64, I64, I, I, I64, P, SZ, P], I),
         "ck_int8_gemm_workspace_size": ([I64, I64, I64], SZ),
@@ -210,6 +213,38 @@ def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stre
     _residual(residual, out_dtype, M, N)
     _check(L.ck_int8_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(residual), _ptr(y), M, N, K, int(mode),
                             code, _ptr(ws), ws.numel(), _stream(stream)))
+    return y
+
+
+def ck_int8_weight_codes(w, w_codes=None, stream=None):
+    """The weight's GEMM operand, once per layer: int8 w [N,K] -> bf16 codes [N,K]."""
+    N, K = w.shape
+    _req(w, torch.int8, (N, K), "w")
+    w_codes = torch.empty((N, K), dtype=torch.bfloat16, device=w.device) if w_codes is None else w_codes
+    _req(w_codes, torch.bfloat16, (N, K), "w_codes")
+    _check(load_library().ck_int8_weight_codes(_ptr(w), N, K, _ptr(w_codes), _stream(stream)))
+    return w_codes
+
+
+def ck_int8_linear_codes(x, w_codes, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stream=None,
+                         out_dtype=torch.bfloat16, residual=None):
+    """ck_int8_linear with the weight given as its bf16 codes (from ck_int8_weight_codes)."""
+    code = _out_code(out_dtype)
+    M, K = x.shape
+    N = w_codes.shape[0]
+    _req(x, torch.bfloat16, (M, K), "x")
+    _req(w_codes, torch.bfloat16, (N, K), "w_codes")
+    _req(w_scale, torch.float32, (1,) if mode == TENSORWISE else (N,), "w_scale")
+    if bias is not None:
+        _req(bias, torch.bfloat16, (N,), "bias")
+    y = torch.empty((M, N), dtype=out_dtype, device=x.device) if y is None else y
+    _req(y, out_dtype, (M, N), "y")
+    L = load_library()
+    need = L.ck_int8_linear_codes_workspace_size(M, N, K, int(mode))
+    ws = workspace(need, x.device) if ws is None else ws
+    _residual(residual, out_dtype, M, N)
+    _check(L.ck_int8_linear_codes(_ptr(x), _ptr(w_codes), _ptr(w_scale), _ptr(bias), _ptr(residual), _ptr(y), M, N,
+                                  K, int(mode), code, _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 

@@ -102,21 +102,24 @@ struct LinearWorkspace {
     void* tail;       // the GEMM's K-split tail: partial sums and arrival slots
 };
 
-size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int mode, int nparts)
+// own_b16: the workspace holds the widened weight (ck_int8_linear); without it the caller
+// passes the weight's codes (ck_int8_linear_codes).
+size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int mode, int nparts, bool own_b16 = true)
 {
-    return align_up((size_t)M * K * 2) + align_up((size_t)N * K * 2) +
+    return align_up((size_t)M * K * 2) + (own_b16 ? align_up((size_t)N * K * 2) : 0) +
            align_up(sizeof(float) * (size_t)(mode == CK_TENSORWISE ? 1 : (M > 0 ? M : 1))) +
            align_up(prep_tensorwise_scratch_bytes(nparts)) + align_up(gemm_tail_bytes(M, N));
 }
 
-LinearWorkspace carve_linear(void* ws, int64_t M, int64_t N, int64_t K, int mode)
+LinearWorkspace carve_linear(void* ws, int64_t M, int64_t N, int64_t K, int mode, bool own_b16 = true)
 {
     uint8_t* p = static_cast<uint8_t*>(ws);
     LinearWorkspace w;
     w.a16 = p;
     p += align_up((size_t)M * K * 2);
-    w.b16 = p;
-    p += align_up((size_t)N * K * 2);
+    w.b16 = own_b16 ? p : nullptr;
+    if (own_b16)
+        p += align_up((size_t)N * K * 2);
     w.xs = reinterpret_cast<float*>(p);
     p += align_up(sizeof(float) * (size_t)(mode == CK_TENSORWISE ? 1 : (M > 0 ? M : 1)));
     w.scratch = p;
@@ -386,9 +389,11 @@ static bool valid_out_dtype(int t)
     return t == CK_OUT_BF16 || t == CK_OUT_F16 || t == CK_OUT_F32;
 }
 
-int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const void* bias, const void* residual,
-                   void* y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype, void* workspace,
-                   size_t workspace_bytes, void* stream)
+// The layer: w8 (int8 codes, widened by the preparation launch) or w_codes (the weight's
+// bf16 codes, prepared once by ck_int8_weight_codes).
+static int linear_impl(const char* name, const void* x, const int8_t* w8, const void* w_codes,
+                       const float* w_scale, const void* bias, const void* residual, void* y, int64_t M, int64_t N,
+                       int64_t K, int mode, int out_dtype, void* workspace, size_t workspace_bytes, void* stream)
 {
     if (mode != CK_TENSORWISE && mode != CK_PER_ROW && mode != CK_CONVROT)
         return fail(CK_ERR_INVALID_ARG, "mode must be 0 (tensorwise), 1 (per-row) or 2 (ConvRot), got %d", mode);
@@ -401,8 +406,12 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
         return fail(CK_ERR_INVALID_ARG, "ConvRot needs K % 128 == 0 (got %lld)", (long long)K);
     if (M == 0)
         return CK_OK;  // empty batch: x and y may be NULL
+    const bool own_b16 = w_codes == nullptr;
     CK_REQUIRE_PTR(x);
-    CK_REQUIRE_PTR(w);
+    if (own_b16)
+        CK_REQUIRE_PTR(w8);
+    else
+        CK_REQUIRE_PTR(w_codes);
     CK_REQUIRE_PTR(w_scale);
     CK_REQUIRE_PTR(y);
     CK_REQUIRE_PTR(workspace);
@@ -410,43 +419,43 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
         return fail(CK_ERR_INVALID_ARG, "bias must be 16-byte aligned");
     if (residual != nullptr && !aligned16(residual))
         return fail(CK_ERR_INVALID_ARG, "residual must be 16-byte aligned");
-    const size_t need = ck_int8_linear_workspace_size(M, N, K, mode);
+    const size_t need = linear_ws_bytes(M, N, K, mode, kMaxPartials, own_b16);
     if (workspace_bytes < need)
         return fail(CK_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
     DeviceInfo dev;
     if ((st = check_device(&dev)) != CK_OK)
         return st;
-    if (M == 0)
-        return CK_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    LinearWorkspace ws = carve_linear(workspace, M, N, K, mode);
+    LinearWorkspace ws = carve_linear(workspace, M, N, K, mode, own_b16);
+    const void* b16 = own_b16 ? ws.b16 : w_codes;
     const bool graph = stream_capturing(s);
     if (log_enabled())
-        log_shape("int8_linear", M, N, K, mode,
-                  std::string(mode == CK_TENSORWISE && graph ? "quantize (2 launches) + widening"
-                                                             : "preparation (1 launch)") +
+        log_shape(name, M, N, K, mode,
+                  std::string(mode == CK_TENSORWISE && graph ? "quantize (2 launches)" : "preparation (1 launch)") +
+                      (own_b16 ? " with the weight widening" : ", weight codes given") +
                       " + tcgen05 bf16-exact GEMM, " + describe_gemm_plan(M, N, K, false, !graph, dev));
     cudaError_t e;
     if (mode == CK_TENSORWISE && graph) {
         // captured: per-block maxima, a quantize pass that reduces them, the widening apart
         ProfScope ps(kProfQuantize, 2, s);
         e = launch_quantize_tensorwise(x, M, K, nullptr, ws.a16, ws.xs, static_cast<float*>(ws.scratch), dev, s);
-        if (e == cudaSuccess)
-            e = launch_widen_int8(w, ws.b16, N * K, dev, s);
+        if (e == cudaSuccess && own_b16)
+            e = launch_widen_int8(w8, ws.b16, N * K, dev, s);
     } else {
-        // one launch: quantize the activation into bf16 codes and widen the weight
+        // one launch: quantize the activation into bf16 codes (and widen the weight)
         ProfScope ps(kProfQuantize, 1, s);
         if (mode == CK_TENSORWISE)
-            e = launch_prep_tensorwise(x, M, K, ws.a16, ws.xs, ws.scratch, kMaxPartialsForLayout, w, N * K, ws.b16,
-                                       dev, s);
+            e = launch_prep_tensorwise(x, M, K, ws.a16, ws.xs, ws.scratch, kMaxPartialsForLayout,
+                                       own_b16 ? w8 : nullptr, N * K, ws.b16, dev, s);
         else
-            e = launch_prep_rows(x, M, K, mode == CK_CONVROT, ws.a16, ws.xs, w, N * K, ws.b16, dev, s);
+            e = launch_prep_rows(x, M, K, mode == CK_CONVROT, ws.a16, ws.xs, own_b16 ? w8 : nullptr, N * K, ws.b16,
+                                 dev, s);
     }
     if (e != cudaSuccess)
-        return cuda_fail(e, "ck_int8_linear preparation launch");
+        return cuda_fail(e, "preparation launch");
     GemmProblem p;
     p.a = ws.a16;
-    p.b = ws.b16;
+    p.b = b16;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -464,8 +473,54 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
         e = launch_gemm(p, dev, s, &why);
     }
     if (e != cudaSuccess)
-        return why.empty() ? cuda_fail(e, "ck_int8_linear GEMM launch") : fail(CK_ERR_CUDA, "%s", why.c_str());
+        return why.empty() ? cuda_fail(e, "GEMM launch") : fail(CK_ERR_CUDA, "%s", why.c_str());
     return CK_OK;
+}
+
+int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const void* bias, const void* residual,
+                   void* y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype, void* workspace,
+                   size_t workspace_bytes, void* stream)
+{
+    return linear_impl("int8_linear", x, w, nullptr, w_scale, bias, residual, y, M, N, K, mode, out_dtype, workspace,
+                       workspace_bytes, stream);
+}
+
+int ck_int8_weight_codes(const int8_t* w, int64_t N, int64_t K, void* w_codes, void* stream)
+{
+    if (N < 0 || K <= 0 || K % 16 != 0)
+        return fail(CK_ERR_INVALID_ARG, "N must be >= 0 and K a positive multiple of 16 (got N=%lld K=%lld)",
+                    (long long)N, (long long)K);
+    if (N > kMaxDim)
+        return fail(CK_ERR_INVALID_ARG, "N must be < 2^31 (got %lld)", (long long)N);
+    if (N == 0)
+        return CK_OK;
+    CK_REQUIRE_PTR(w);
+    CK_REQUIRE_PTR(w_codes);
+    DeviceInfo dev;
+    int st = check_device(&dev);
+    if (st != CK_OK)
+        return st;
+    cudaError_t e;
+    {
+        ProfScope ps(kProfWiden, 1, static_cast<cudaStream_t>(stream));
+        e = launch_widen_int8(w, w_codes, N * K, dev, static_cast<cudaStream_t>(stream));
+    }
+    return e == cudaSuccess ? CK_OK : cuda_fail(e, "ck_int8_weight_codes launch");
+}
+
+size_t ck_int8_linear_codes_workspace_size(int64_t M, int64_t N, int64_t K, int mode)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return 0;
+    return linear_ws_bytes(M, N, K, mode, kMaxPartials, false);
+}
+
+int ck_int8_linear_codes(const void* x, const void* w_codes, const float* w_scale, const void* bias,
+                         const void* residual, void* y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype,
+                         void* workspace, size_t workspace_bytes, void* stream)
+{
+    return linear_impl("int8_linear_codes", x, nullptr, w_codes, w_scale, bias, residual, y, M, N, K, mode, out_dtype,
+                       workspace, workspace_bytes, stream);
 }
 
 // ---- the 16-bit-activation path --------------------------------------------------

@@ -159,3 +159,35 @@ def test_linear_residual_in_place(mode):
     assert_guards_intact(ybuf, NAN16)
     d = bf16_ulp_distance(bits(y), ref)
     assert d.max() <= MAX_ULP, "max ulp %d" % d.max()
+
+
+@pytest.mark.parametrize("mode", [synthetic.TENSORWISE, synthetic.PER_ROW, synthetic.CONVROT])
+def test_linear_with_prepared_weight_codes(mode):
+    """The weight's codes prepared once (ck_int8_weight_codes) and the layer run on them
+    (ck_int8_linear_codes): the codes equal the int8 weight, and every output equals
+    ck_int8_linear's and the oracle's, two calls in a row."""
+    M, N, K = 1000, 776, 1152
+    x = synthetic.normal_bf16((M, K), seed=81 + mode)
+    if mode == synthetic.CONVROT:
+        w, ws = oracle.prepare_convrot_weight(synthetic.normal_f32((N, K), seed=82, std=0.02).numpy())
+        w, ws = torch.from_numpy(w), torch.from_numpy(ws)
+    else:
+        w = synthetic.int8_uniform((N, K), seed=82)
+        ws = synthetic.scale_uniform(1 if mode == synthetic.TENSORWISE else N, seed=83)
+    b = synthetic.normal_bf16((1, N), seed=84, std=0.5).reshape(N)
+    wd, wsd, bd = w.to(DEV), ws.to(DEV), b.to(DEV)
+    cbuf, codes = guarded((N, K), torch.bfloat16, NAN16)
+    ck.ck_int8_weight_codes(wd, w_codes=codes)
+    torch.cuda.synchronize()
+    assert_guards_intact(cbuf, NAN16)
+    assert torch.equal(codes.float().cpu(), w.float())
+    want = oracle.int8_linear(bits(x), w.numpy(), ws.numpy(), bits(b), mode=mode)["y"]
+    xd = x.to(DEV)
+    ref = bits(ck.ck_int8_linear(xd, wd, wsd, bd, mode=mode))
+    for _ in range(2):
+        ybuf, y = guarded((M, N), torch.bfloat16, NAN16)
+        ck.ck_int8_linear_codes(xd, codes, wsd, bd, mode=mode, y=y)
+        torch.cuda.synchronize()
+        assert_guards_intact(ybuf, NAN16)
+        assert np.array_equal(bits(y), ref)
+        assert bf16_ulp_distance(bits(y), want).max() <= MAX_ULP
