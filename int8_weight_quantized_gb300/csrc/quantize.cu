@@ -79,6 +79,16 @@ __device__ __forceinline__ __nv_bfloat162 absmax8(__nv_bfloat162 m, const uint4&
 // quarter-rate conversion instructions, which at HBM speed would be its bottleneck.
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 
+// Two fp32 values per instruction (sm_100-family packed FP32): each lane of a packed
+// add, multiply or fma rounds exactly like the scalar instruction, so a packed step is
+// the same IEEE operation on both values at half the issue cost.  a - b is formed as
+// fma(b, -1, a): the product by -1 is exact, so it is a - b rounded once.
+__device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, dup2(-1.0f), a); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
 // x_scale = fl(amax / 127) for amax >= 0 finite, without a division: q1 = fl(amax * c)
 // with c = fl(1/127), then one FMA correction of the remainder (Markstein, IBM J. Res.
 // Dev. 34(1), 1990).  The result equals the correctly rounded quotient for every
@@ -145,7 +155,28 @@ struct Coder {
             return slow(v);
         return kRoundMagic;
     }
+    // kind 1 on two values: magic1's steps, packed
+    __device__ __forceinline__ float2 magic1x2(float2 v) const
+    {
+        float2 t = mul2(v, dup2(r));
+        const float2 e = fma2(t, dup2(-s), v);  // t * (-s) is -(t * s) exactly
+        t = fma2(e, dup2(r), t);
+        return add2(t, dup2(kRoundMagic));
+    }
+    // kind 3 on two values, without the near-tie test: the magic sum of t = v * r, and
+    // d = t - rint(t) (exact: Fast2Sum against kRoundMagic, then Sterbenz).  |d| <= 1/2,
+    // and magic3's test |(|d| - 1/2)| <= 2^-14 is |d| >= 1/2 - 2^-14 (the subtraction is
+    // exact for |d| >= 1/4); a caller that finds such a d redoes those values by magic3.
+    __device__ __forceinline__ float2 magic3x2(float2 v, float& dmax) const
+    {
+        const float2 t = mul2(v, dup2(r));
+        const float2 m = add2(t, dup2(kRoundMagic));
+        const float2 d = sub2(t, add2(m, dup2(-kRoundMagic)));
+        dmax = fmaxf(dmax, fmaxf(fabsf(d.x), fabsf(d.y)));
+        return m;
+    }
 };
+constexpr float kNearTie = 0.5f - 0x1p-14f;  // magic3's near-tie bound on |t - rint(t)|
 
 // Eight codes from eight magic sums: int8 bytes, or bf16 codes.
 template <bool OUT8>
@@ -162,9 +193,10 @@ __device__ __forceinline__ void store_magic8(const float (&m)[8], int8_t* q8, __
     } else {
         uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            w[i] = __byte_perm(__float_as_uint(__fsub_rn(m[2 * i], kRoundMagic)),
-                               __float_as_uint(__fsub_rn(m[2 * i + 1], kRoundMagic)), 0x7632);
+        for (int i = 0; i < 4; ++i) {
+            const float2 n = add2(make_float2(m[2 * i], m[2 * i + 1]), dup2(-kRoundMagic));
+            w[i] = __byte_perm(__float_as_uint(n.x), __float_as_uint(n.y), 0x7632);
+        }
         *reinterpret_cast<uint4*>(q16 + off) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
@@ -177,15 +209,26 @@ __device__ __forceinline__ void code_store8(const Coder& cd, const float (&f)[8]
                                             int64_t off)
 {
     float m[8];
+    bool done = false;
     if (cd.kind == 1) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            m[e] = cd.magic1(f[e]);
+        for (int i = 0; i < 4; ++i) {
+            const float2 mm = cd.magic1x2(make_float2(f[2 * i], f[2 * i + 1]));
+            m[2 * i] = mm.x;
+            m[2 * i + 1] = mm.y;
+        }
+        done = true;
     } else if (cd.kind == 3) {
+        float dmax = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            m[e] = cd.magic3(f[e]);
-    } else {
+        for (int i = 0; i < 4; ++i) {
+            const float2 mm = cd.magic3x2(make_float2(f[2 * i], f[2 * i + 1]), dmax);
+            m[2 * i] = mm.x;
+            m[2 * i + 1] = mm.y;
+        }
+        done = dmax < kNearTie;
+    }
+    if (!done) {
         for (int e = 0; e < 8; ++e)
             m[e] = cd.magic(f[e]);
     }
@@ -255,6 +298,91 @@ __device__ __forceinline__ void fwht_slot(float (&v)[8], int lane)
 #pragma unroll
     for (int e = 0; e < 8; ++e)
         v[e] = __fmul_rn(v[e], c128);
+}
+
+// The same transform on two vector slots of a lane at once: element e of slot a in
+// v[e].x, of slot b in v[e].y.  Every butterfly is the scalar one, two values per packed
+// instruction (a - b as fma(b, -1, a), exact product), in the same span order.
+__device__ __forceinline__ void fwht_pair(float2 (&v)[8], int lane)
+{
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if ((e & h) == 0) {
+                const float2 lo = v[e], hi = v[e + h];
+                v[e] = add2(lo, hi);
+                v[e + h] = sub2(lo, hi);
+            }
+        }
+    }
+#pragma unroll
+    for (int hl = 1; hl < 16; hl <<= 1) {
+        const float2 sgn = dup2((lane & hl) ? -1.0f : 1.0f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float2 p = make_float2(__shfl_xor_sync(0xffffffffu, v[e].x, hl),
+                                         __shfl_xor_sync(0xffffffffu, v[e].y, hl));
+            v[e] = fma2(sgn, v[e], p);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        v[e] = mul2(v[e], dup2(0.088388346f));  // fp32(1/sqrt(128)), as in fwht_slot
+}
+
+// The codes of two slots (element e of slot a in v[e].x, of slot b in v[e].y) by the rule
+// of `cd`, stored at element offsets off_a / off_b where st_a / st_b hold.  The scale's
+// rule is the same for both (one row).
+template <bool OUT8, bool OUT16>
+__device__ __forceinline__ void code_store_pair(const Coder& cd, const float2 (&v)[8], int8_t* q8,
+                                                __nv_bfloat16* q16, int64_t off_a, bool st_a, int64_t off_b,
+                                                bool st_b)
+{
+    float2 m[8];
+    bool done = false;
+    if (cd.kind == 3) {
+        float dmax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            m[e] = cd.magic3x2(v[e], dmax);
+        done = dmax < kNearTie;
+    } else if (cd.kind == 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            m[e] = cd.magic1x2(v[e]);
+        done = true;
+    }
+    if (!done) {
+        for (int e = 0; e < 8; ++e)
+            m[e] = make_float2(cd.magic(v[e].x), cd.magic(v[e].y));
+    }
+    if (OUT8) {
+        float ma[8], mb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            ma[e] = m[e].x;
+            mb[e] = m[e].y;
+        }
+        if (st_a)
+            store_magic8<true>(ma, q8, nullptr, off_a);
+        if (st_b)
+            store_magic8<true>(mb, q8, nullptr, off_b);
+    }
+    if (OUT16) {
+        uint32_t wa[4], wb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 n0 = add2(m[2 * i], dup2(-kRoundMagic));
+            const float2 n1 = add2(m[2 * i + 1], dup2(-kRoundMagic));
+            wa[i] = __byte_perm(__float_as_uint(n0.x), __float_as_uint(n1.x), 0x7632);
+            wb[i] = __byte_perm(__float_as_uint(n0.y), __float_as_uint(n1.y), 0x7632);
+        }
+        if (st_a)
+            *reinterpret_cast<uint4*>(q16 + off_a) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        if (st_b)
+            *reinterpret_cast<uint4*>(q16 + off_b) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+    }
 }
 
 // int8 -> bf16 (exact), 16 values per thread and vector.
@@ -336,7 +464,12 @@ __global__ void __launch_bounds__(THREADS) rows_kernel(const uint4* __restrict__
     const uint4* xr = x + (live ? row : 0) * nvec;
     const int64_t warp_first = t - lane;  // first vector of this warp in slot 0
 
-    float v[VPT][8];
+    // ConvRot: slots 2i and 2i + 1 are transformed together (packed pairs); an odd
+    // VPT leaves the last slot to the scalar transform
+    constexpr int NP = ROT ? VPT / 2 : 0;
+    constexpr int NS = ROT ? VPT % 2 : 0;
+    float2 vp[NP > 0 ? NP : 1][8];
+    float vs[8];
     uint4 raw[VPT];
     float amax = 0.0f;
     __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
@@ -349,13 +482,29 @@ __global__ void __launch_bounds__(THREADS) rows_kernel(const uint4* __restrict__
     }
     if (ROT) {
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            unpack8_bits(raw[j], v[j]);
-            if (warp_first + (int64_t)TPR * j < nvec) {  // warp-uniform
-                fwht_slot(v[j], lane);
+        for (int i = 0; i < NP; ++i) {
+            // slot 2i + 1 of the warp may lie past the row while slot 2i does not: its
+            // values are zeros then, which leave the maximum alone
+            if (warp_first + (int64_t)TPR * (2 * i) < nvec) {  // warp-uniform
+                float fa[8], fb[8];
+                unpack8_bits(raw[2 * i], fa);
+                unpack8_bits(raw[2 * i + 1], fb);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    amax = fmaxf(amax, fabsf(v[j][e]));
+                    vp[i][e] = make_float2(fa[e], fb[e]);
+                fwht_pair(vp[i], lane);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    amax = fmaxf(amax, fmaxf(fabsf(vp[i][e].x), fabsf(vp[i][e].y)));
+            }
+        }
+        if (NS) {
+            unpack8_bits(raw[VPT - 1], vs);
+            if (warp_first + (int64_t)TPR * (VPT - 1) < nvec) {  // warp-uniform
+                fwht_slot(vs, lane);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    amax = fmaxf(amax, fabsf(vs[e]));
             }
         }
     } else {
@@ -375,13 +524,24 @@ __global__ void __launch_bounds__(THREADS) rows_kernel(const uint4* __restrict__
         if (t == 0)
             xs[row] = s;
         const Coder cd(s, ROT);
+        if (ROT) {
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int64_t idx = t + (int64_t)TPR * j;
-            if (idx < nvec) {
-                if (ROT) {
-                    code_store8<OUT8, OUT16>(cd, v[j], q8, q16, row * K + idx * 8);
-                } else {
+            for (int i = 0; i < NP; ++i) {
+                const int64_t ia = t + (int64_t)TPR * (2 * i), ib = ia + TPR;
+                if (ia < nvec)
+                    code_store_pair<OUT8, OUT16>(cd, vp[i], q8, q16, row * K + ia * 8, true, row * K + ib * 8,
+                                                 ib < nvec);
+            }
+            if (NS) {
+                const int64_t idx = t + (int64_t)TPR * (VPT - 1);
+                if (idx < nvec)
+                    code_store8<OUT8, OUT16>(cd, vs, q8, q16, row * K + idx * 8);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int64_t idx = t + (int64_t)TPR * j;
+                if (idx < nvec) {
                     float f[8];
                     unpack8_bits(raw[j], f);
                     code_store8<OUT8, OUT16>(cd, f, q8, q16, row * K + idx * 8);
