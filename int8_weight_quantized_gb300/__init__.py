@@ -84,19 +84,28 @@ def _check(status):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: the c_void_p argument types convert it (0 / None is NULL)
+    return None if t is None else t.data_ptr()
+
+
+# The current stream's handle without building a torch Stream object (that costs ~3 us a
+# call, as much as a kernel launch); the public route where the fast one is missing.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
 
 
 def _stream(stream):
     if stream is None:
+        if _raw_stream is not None and _cur_device is not None:
+            return _raw_stream(_cur_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _req(t, dtype, shape, name):
     if t.dtype != dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
@@ -139,8 +148,8 @@ def ck_quantize_int8_tensorwise(x, q=None, x_scale=None, ws=None, stream=None):
     _req(q, torch.int8, (M, K), "q")
     _req(x_scale, torch.float32, (1,), "x_scale")
     L = load_library()
-    need = L.ck_quantize_tensorwise_workspace_size()
-    ws = workspace(need, x.device) if ws is None else ws
+    if ws is None:
+        ws = workspace(L.ck_quantize_tensorwise_workspace_size(), x.device)
     _check(L.ck_quantize_int8_tensorwise(_ptr(x), M, K, _ptr(q), _ptr(x_scale), _ptr(ws), ws.numel(),
                                          _stream(stream)))
     return q, x_scale
@@ -208,8 +217,8 @@ def ck_int8_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, stre
     y = torch.empty((M, N), dtype=out_dtype, device=x.device) if y is None else y
     _req(y, out_dtype, (M, N), "y")
     L = load_library()
-    need = L.ck_int8_linear_workspace_size(M, N, K, int(mode))
-    ws = workspace(need, x.device) if ws is None else ws
+    if ws is None:  # a workspace the caller gives is checked for size by the library
+        ws = workspace(L.ck_int8_linear_workspace_size(M, N, K, int(mode)), x.device)
     _residual(residual, out_dtype, M, N)
     _check(L.ck_int8_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(residual), _ptr(y), M, N, K, int(mode),
                             code, _ptr(ws), ws.numel(), _stream(stream)))
@@ -240,8 +249,8 @@ def ck_int8_linear_codes(x, w_codes, w_scale, bias=None, mode=PER_ROW, y=None, w
     y = torch.empty((M, N), dtype=out_dtype, device=x.device) if y is None else y
     _req(y, out_dtype, (M, N), "y")
     L = load_library()
-    need = L.ck_int8_linear_codes_workspace_size(M, N, K, int(mode))
-    ws = workspace(need, x.device) if ws is None else ws
+    if ws is None:
+        ws = workspace(L.ck_int8_linear_codes_workspace_size(M, N, K, int(mode)), x.device)
     _residual(residual, out_dtype, M, N)
     _check(L.ck_int8_linear_codes(_ptr(x), _ptr(w_codes), _ptr(w_scale), _ptr(bias), _ptr(residual), _ptr(y), M, N,
                                   K, int(mode), code, _ptr(ws), ws.numel(), _stream(stream)))
@@ -267,8 +276,8 @@ def ck_int8_linear_host(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None,
     if y.dtype != out_dtype or tuple(y.shape) != (M, N) or y.is_cuda or not y.is_contiguous():
         raise ValueError("y must be a contiguous host tensor of shape %s and type %s" % ((M, N), out_dtype))
     L = load_library()
-    need = L.ck_int8_linear_host_workspace_size(M, N, K, int(mode), code, int(slab_rows))
-    ws = workspace(need, w.device) if ws is None else ws
+    if ws is None:
+        ws = workspace(L.ck_int8_linear_host_workspace_size(M, N, K, int(mode), code, int(slab_rows)), w.device)
     _check(L.ck_int8_linear_host(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, int(mode), code,
                                  int(slab_rows), _ptr(ws), ws.numel(), _stream(stream)))
     return y
@@ -288,8 +297,8 @@ def ck_w8a16_linear(x, w, w_scale, bias=None, mode=PER_ROW, y=None, ws=None, str
     y = torch.empty((M, N), dtype=out_dtype, device=x.device) if y is None else y
     _req(y, out_dtype, (M, N), "y")
     L = load_library()
-    need = L.ck_w8a16_linear_workspace_size(M, N, K, int(mode))
-    ws = workspace(need, x.device) if ws is None else ws
+    if ws is None:
+        ws = workspace(L.ck_w8a16_linear_workspace_size(M, N, K, int(mode)), x.device)
     _residual(residual, out_dtype, M, N)
     _check(L.ck_w8a16_linear(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(residual), _ptr(y), M, N, K,
                              int(mode), code, _ptr(ws), ws.numel(), _stream(stream)))
@@ -323,8 +332,8 @@ def ck_int8_gemm_dequant(q, x_scale, w, w_scale, bias=None, scalar_scales=False,
     y = torch.empty((M, N), dtype=out_dtype, device=q.device) if y is None else y
     _req(y, out_dtype, (M, N), "y")
     L = load_library()
-    need = L.ck_int8_gemm_workspace_size(M, N, K)
-    ws = workspace(need, q.device) if ws is None else ws
+    if ws is None:
+        ws = workspace(L.ck_int8_gemm_workspace_size(M, N, K), q.device)
     _residual(residual, out_dtype, M, N)
     _check(L.ck_int8_gemm_dequant(_ptr(q), _ptr(x_scale), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(residual), _ptr(y),
                                   M, N, K, int(bool(scalar_scales)), code, _ptr(ws), ws.numel(), _stream(stream)))
@@ -340,8 +349,8 @@ def ck_int8_gemm_s32(q, w, acc=None, ws=None, stream=None):
     acc = torch.empty((M, N), dtype=torch.int32, device=q.device) if acc is None else acc
     _req(acc, torch.int32, (M, N), "acc")
     L = load_library()
-    need = L.ck_int8_gemm_workspace_size(M, N, K)
-    ws = workspace(need, q.device) if ws is None else ws
+    if ws is None:
+        ws = workspace(L.ck_int8_gemm_workspace_size(M, N, K), q.device)
     _check(L.ck_int8_gemm_s32(_ptr(q), _ptr(w), _ptr(acc), M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
     return acc
 
