@@ -118,3 +118,20 @@ def test_consecutive_calls_leave_nothing_behind(mode):
         y, codes, xs = layer_and_codes(x, w, ws, b, mode, work)
         check_codes(codes, xs, ref, mode)
         assert bf16_ulp_distance(bits(y), ref["y"]).max() <= MAX_ULP
+
+
+@pytest.mark.parametrize("K", [1152, 3072])
+def test_convrot_layer_codes_at_half_integer_quotients(K):
+    """The layer's ConvRot preparation (bf16 codes) on rows whose rotated values all sit
+    within fp32 rounding of half-integer multiples of the scale (the construction of
+    test_gpu_quantize._half_integer_rows): every code is decided by the quotient's last
+    bits and must equal the oracle's."""
+    from test_gpu_quantize import _half_integer_rows
+    M, N = 200, 128
+    x = _half_integer_rows(M, K, seed=K)
+    _, w, ws, b = case_inputs(M, N, K, CR, seed=K + 1)
+    ref = oracle.int8_linear(bits(x), w.numpy(), ws.numpy(), bits(b), mode=CR)
+    work = torch.empty(ck.ck_int8_linear_workspace_size(M, N, K, CR), dtype=torch.uint8, device=DEV)
+    y, codes, xs = layer_and_codes(x, w, ws, b, CR, work)
+    check_codes(codes, xs, ref, CR)
+    assert bf16_ulp_distance(bits(y), ref["y"]).max() <= MAX_ULP

@@ -2,6 +2,7 @@
 fp32 scales must be bit-identical (integer decisions taken in fp32 on both sides)."""
 import numpy as np
 import pytest
+import scipy.linalg
 import torch
 
 import oracle
@@ -146,3 +147,48 @@ def test_every_bf16_row_maximum():
     third = (torch.from_numpy(amax.view(np.int16)).view(torch.bfloat16).float() / 3).to(torch.bfloat16)
     xb[:, 2] = bits(third)
     check_rowwise(from_bits(xb), rotate=False)
+
+
+def _half_integer_rows(M, K, seed):
+    """bf16 rows whose rotated values all sit within fp32 rounding of a half-integer
+    multiple of the row's scale: block 0 holds 254 at one position (its transform is
+    +-254/sqrt(128) everywhere, the row maximum, so x_scale is about 2/sqrt(128)); every
+    other 128-block holds two integers a, b with a + b odd, whose transform is
+    +-(a + b)/sqrt(128) or +-(a - b)/sqrt(128), i.e. (a +- b)/2 in units of the scale."""
+    rng = np.random.default_rng(seed)
+    x = np.zeros((M, K), np.float32)
+    for m in range(M):
+        x[m, rng.integers(0, 128)] = 254.0 * (1 if m % 2 else -1)
+        for blk in range(1, K // 128):
+            p1, p2 = rng.choice(128, 2, replace=False)
+            a = int(rng.integers(-127, 128))
+            b = int(rng.integers(-127, 127))
+            if (a + b) % 2 == 0:
+                b += 1
+            x[m, blk * 128 + p1], x[m, blk * 128 + p2] = a, b
+    return torch.from_numpy(x).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("M,K", [(64, 1024), (48, 3072), (16, 4096), (8, 16384)])
+def test_convrot_half_integer_quotients(M, K):
+    """Nearly every code of these rows is decided by the last bits of the quotient (the
+    near-tie branch of the ConvRot rounding, packed and scalar slots alike): the GPU codes
+    and scales must still equal the oracle's IEEE division."""
+    x = _half_integer_rows(M, K, seed=K + M)
+    _, s_ref = oracle.quantize_rowwise(bits(x), rotate=True)
+    # the quotients in exact arithmetic (float64 transform): within 2^-12 of a half-integer
+    H = scipy.linalg.hadamard(128) / np.sqrt(128.0)
+    v = (x.double().numpy().reshape(M, K // 128, 128) @ H).reshape(M, K)[:, 128:]
+    t = np.abs(v / s_ref.astype(np.float64)[:, None])
+    assert (np.abs(t - np.floor(t) - 0.5) < 2.0 ** -12).mean() > 0.95
+    check_rowwise(x, rotate=True)
+
+
+def test_convrot_weight_half_integer_quotients():
+    """The same construction through the ConvRot weight preparation (fp32 rows)."""
+    W = _half_integer_rows(96, 1024, seed=3).float()
+    w_ref, s_ref = oracle.prepare_convrot_weight(W.numpy())
+    w, s = ck.ck_convrot_prepare_weight(W.to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(w.cpu().numpy(), w_ref)
