@@ -32,6 +32,46 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// ---------------------------------------------------------------- packed fp32 (two values per instruction)
+// sm_100-family GPUs execute two fp32 adds, multiplies or fmas as one instruction, each
+// lane rounded exactly like the scalar one.  The rounding mode is spelled out (.rn):
+// an add or multiply with an explicit rounding modifier is never contracted into an fma
+// with a neighbouring instruction, so a multiply followed by an add stays two roundings,
+// as the scalar __fmul_rn / __fadd_rn would.
+__device__ __forceinline__ float2 f2_add_rn(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "add.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 f2_mul_rn(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// a * b + c, one rounding per lane
+__device__ __forceinline__ float2 f2_fma_rn(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\tmov.b64 pc, {%6, %7};\n\t"
+        "fma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // A kernel launched with programmatic stream serialization may start while its
 // predecessor on the stream is still running; griddep_wait() blocks until that

@@ -124,6 +124,7 @@ struct Args {
     uint32_t tx_bytes;      // bytes of one k-block counted on the (leader's) full barrier
     int units_m, tiles_m, tiles_n, num_kb, group_m;
     int scalar_scales;
+    float one;              // 1.0f, a value the compiler cannot see (the epilogue's packed adds)
     int chunk_kb;           // k-blocks per TMEM accumulation: 1024 products (exact), all of K (16-bit activations)
     uint64_t timeout_ns;
     // K-split of the last partial wave: units [full_units, num_units) are each computed
@@ -567,20 +568,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // both accumulators to fill and the MMAs to stall.  Each box converts
                 // run[0 .. BOX) and shifts the sums down by BOX, so indices stay compile-time.
 #pragma unroll 1
-                for (int g = 0; g < 128 / BOX; ++g) {
+                for (int g2 = 0; g2 < 128 / BOX; g2 += 2) {
+                  bool stop = false;
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {  // two boxes per pass: run[h * BOX ..]
+                    const int g = g2 + h;
                     const int64_t col0 = cbase + g * OT::BOX_COLS;
-                    if (g * OT::BOX_COLS >= ncols || col0 >= args.N || row0 >= args.M)
-                        break;  // warp-uniform: nothing of this box is inside the tile and y
+                    if (g * OT::BOX_COLS >= ncols || col0 >= args.N || row0 >= args.M) {
+                        stop = true;  // warp-uniform: nothing of this box is inside the tile and y
+                        break;
+                    }
                     uint8_t* buf = obuf + (nstore & 1u) * OUT_BUF_BYTES;
                     if (lane == 0)
                         bulk_wait_group_read<1>();  // the store that last used `buf` has read it
                     __syncwarp();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {  // one 16-byte chunk of the row: PC columns
-                        const int j0 = c * PC;  // first running sum of the chunk (after the shifts)
+                        const int j0 = h * BOX + c * PC;  // first running sum of the chunk (after the shifts)
                         const int64_t col = col0 + c * PC;
-                        // the same columns for every lane: broadcast loads, L1 hits after the
-                        // first tile of a column range
                         // the columns' w_scale and bias from the lanes that loaded them (columns
                         // past N hold 0: computed, then clipped by the store)
                         float wsv[PC], bv[PC];
@@ -601,20 +606,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                             for (int i = 0; i < PC; ++i)
                                 rv[i] = 0.0f;
                         }
+                        // two columns per packed fp32x2 instruction, each lane rounded like the
+                        // scalar __fmul_rn / __fadd_rn, in the same order.  The adds are
+                        // fma(u, one, v): a packed add taking a packed product with no other use
+                        // was fused into one fma by the compiler (CUDA 13.0, sm_103a: despite .rn
+                        // and -fmad=false), which rounds once where the layer rounds twice; an
+                        // fma by a 1.0 the compiler cannot see is exactly the add, never fused.
+                        const float2 one2 = make_float2(args.one, args.one);
                         float t[PC];
 #pragma unroll
-                        for (int i = 0; i < PC; ++i) {
+                        for (int i = 0; i < PC; i += 2) {
+                            float2 u;
                             if (MIXED) {  // 16-bit activations: (sum * w_scale) + bias
-                                t[i] = __int_as_float(run[j0 + i]);
+                                u = make_float2(__int_as_float(run[j0 + i]), __int_as_float(run[j0 + i + 1]));
                             } else {
-                                t[i] = __int2float_rn(run[j0 + i]);
-                                t[i] = __fmul_rn(t[i], xsv);
+                                u = make_float2(__int2float_rn(run[j0 + i]), __int2float_rn(run[j0 + i + 1]));
+                                u = f2_mul_rn(u, make_float2(xsv, xsv));
                             }
-                            t[i] = __fmul_rn(t[i], wsv[i]);
+                            u = f2_mul_rn(u, make_float2(wsv[i], wsv[i + 1]));
                             if (args.bias)
-                                t[i] = __fadd_rn(t[i], bv[i]);
+                                u = f2_fma_rn(u, one2, make_float2(bv[i], bv[i + 1]));
                             if (RES)
-                                t[i] = __fadd_rn(t[i], rv[i]);
+                                u = f2_fma_rn(u, one2, make_float2(rv[i], rv[i + 1]));
+                            t[i] = u.x;
+                            t[i + 1] = u.y;
                         }
                         uint32_t packed[4];
                         if (OUT == kOutF32) {
@@ -638,9 +653,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         bulk_commit_group();
                     }
                     ++nstore;
+                  }
+                  if (stop)
+                      break;
 #pragma unroll
-                    for (int j = 0; j < 128 - BOX; ++j)
-                        run[j] = run[j + BOX];
+                  for (int j = 0; j < 128 - 2 * BOX; ++j)
+                      run[j] = run[j + 2 * BOX];
                 }
             }
         }
@@ -1047,6 +1065,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.tiles_m = (int)((p.M + BM - 1) / BM);
     a.scalar_scales = p.scalar_scales;
     a.timeout_ns = DEFAULT_TIMEOUT_NS;
+    a.one = 1.0f;
     GemmPlan plan;
     const cudaError_t e = plan_gemm(p.M, p.N, p.K, p.mixed, dev, &plan);
     if (e != cudaSuccess)

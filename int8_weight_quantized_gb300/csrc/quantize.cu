@@ -79,15 +79,15 @@ __device__ __forceinline__ __nv_bfloat162 absmax8(__nv_bfloat162 m, const uint4&
 // quarter-rate conversion instructions, which at HBM speed would be its bottleneck.
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 
-// Two fp32 values per instruction (sm_100-family packed FP32): each lane of a packed
-// add, multiply or fma rounds exactly like the scalar instruction, so a packed step is
-// the same IEEE operation on both values at half the issue cost.  a - b is formed as
+// Two fp32 values per instruction (the packed helpers of ck_device.cuh): each lane
+// rounds exactly like the scalar instruction and nothing is contracted, so a packed step
+// is the same IEEE operation on both values at half the issue cost.  a - b is formed as
 // fma(b, -1, a): the product by -1 is exact, so it is a - b rounded once.
 __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, dup2(-1.0f), a); }
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return f2_add_rn(a, b); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return f2_fma_rn(b, dup2(-1.0f), a); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return f2_mul_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return f2_fma_rn(a, b, c); }
 
 // x_scale = fl(amax / 127) for amax >= 0 finite, without a division: q1 = fl(amax * c)
 // with c = fl(1/127), then one FMA correction of the remainder (Markstein, IBM J. Res.
@@ -167,6 +167,10 @@ struct Coder {
     // d = t - rint(t) (exact: Fast2Sum against kRoundMagic, then Sterbenz).  |d| <= 1/2,
     // and magic3's test |(|d| - 1/2)| <= 2^-14 is |d| >= 1/2 - 2^-14 (the subtraction is
     // exact for |d| >= 1/4); a caller that finds such a d redoes those values by magic3.
+    // Should the compiler fuse the product into the magic add (it has fused a packed add
+    // with a packed product of single use), the sum rounds v * r exactly instead of t; the
+    // two differ only if t lies within half an ulp (<= 2^-18) of a half-integer, and then
+    // d is at least 1/2 away from the integer taken, so those values take magic3 as well.
     __device__ __forceinline__ float2 magic3x2(float2 v, float& dmax) const
     {
         const float2 t = mul2(v, dup2(r));
