@@ -1075,16 +1075,20 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.units_m = (a.tiles_m + a.unit_rows - 1) / a.unit_rows;
     // Grouped order: the resident units sweep N together over a band of tile rows.  When
     // both operands fit in L2 together (up to 80 MB of bf16 codes) a 1024-row band is
-    // best; larger problems take a band of about 24 MB of activation rows (1024 to 4096
+    // best; larger problems take a band of about 32 MB of activation rows (1024 to 4096
     // rows), which stays in L2 while the weight streams past it, so the weight is read
-    // from HBM about once per band.  Measured on GB300 (interleaved runs, against the
-    // 1024-row band): 4096x12288x3072 0.180 -> 0.168 ms, 8192x16384x4096 0.579 -> 0.541,
-    // 25900x16384x4096 1.869 -> 1.772, 80666x28672x5376 13.95 -> 13.52, 99865x21504x5376
-    // 12.66 -> 12.24; 4096^3 was 3.7% slower with the wider band and keeps 1024 rows.
+    // from HBM about once per band.  Measured on GB300 (interleaved runs), a 24 MB band
+    // against the 1024-row one: 4096x12288x3072 0.180 -> 0.168 ms, 8192x16384x4096 0.579 ->
+    // 0.541, 25900x16384x4096 1.869 -> 1.772, 80666x28672x5376 13.95 -> 13.52,
+    // 99865x21504x5376 12.66 -> 12.24 (4096^3 was 3.7% slower with the wider band and keeps
+    // 1024 rows); 32 MB against 24 MB, GEMM launches under the power cap: 80666x28672x5376
+    // 13.39 -> 13.20 ms, 99865x21504x5376 12.51 -> 12.24, 8192x16384x4096 0.531 -> 0.530,
+    // 25900x16384x4096 1.74 -> 1.73; wider bands lose the weight's reuse in L2 (80666x28672x5376:
+    // 38 MB 13.23 ms, 50 MB 13.55, 66 MB 14.3).
     // CK_GEMM_GROUP=<units per band> overrides (A/B timing).
     const bool fits_l2 = 2 * p.K * (p.M + p.N) <= ((int64_t)80 << 20);
     const int64_t band_rows =
-        fits_l2 ? 1024 : std::min<int64_t>(4096, std::max<int64_t>(1024, ((int64_t)24 << 20) / (2 * p.K)));
+        fits_l2 ? 1024 : std::min<int64_t>(4096, std::max<int64_t>(1024, ((int64_t)32 << 20) / (2 * p.K)));
     a.group_m = (int)std::max<int64_t>(1, band_rows / (pair ? 2 * BM : BM));
     if (const char* g = std::getenv("CK_GEMM_GROUP")) {  // unit rows per sweep over N (A/B timing)
         const int v = std::atoi(g);
