@@ -36,10 +36,12 @@ def check_rowwise(x_cpu, rotate):
         len(bad), bad[0], qn[tuple(bad[0])], q_ref[tuple(bad[0])])
 
 
-# register-resident paths for every threads-per-row choice (32..256 threads, 4 or 8
-# vectors each: K up to 16384), ragged row tails, and the two-pass path for longer rows
-@pytest.mark.parametrize("M,K", [(256, 512), (37, 16), (9, 48), (100, 2048), (3, 6144), (5, 5376),
-                                 (7, 6160), (13, 4096), (3, 12288), (2, 16384), (2, 16400), (2, 65536)])
+# register-resident paths for every threads-per-row choice of the plain rows (32 x 2/4/8,
+# 64 x 6/8, 128 x 6/8, 256 x 6/8: K up to 16384), ragged row tails, and the two-pass path
+# for longer rows
+@pytest.mark.parametrize("M,K", [(256, 512), (37, 16), (9, 48), (21, 1024), (100, 2048), (11, 3072), (3, 6144),
+                                 (5, 5376), (7, 6160), (13, 4096), (9, 8192), (3, 12288), (2, 16384), (2, 16400),
+                                 (2, 65536)])
 def test_rowwise_parity(M, K):
     check_rowwise(synthetic.normal_bf16((M, K), seed=100 + K), rotate=False)
 
