@@ -1064,13 +1064,17 @@ cudaError_t rows_dispatch(const void* x, int64_t M, int64_t K, bool rotate, int8
     // threads per row (32..256) and vectors per thread (at most 8: rows up to K = 16384
     // stay in registers), chosen so that few of the tpr * vpt vector slots stay empty:
     // idle slots cost bandwidth (K = 5376, 672 vectors, in 256 x 4 slots ran at 81% of
-    // HBM, in 128 x 6 at 98%).  Plain rows take as many vectors per thread as fill (the
-    // loads a thread has in flight are what keeps HBM busy: K = 4096 as 64 x 8 instead of
-    // 128 x 4 went 0.91 -> 1.00 of HBM on 25900 rows, K = 2048 as 32 x 8 instead of 64 x 4
-    // 0.73 -> 0.87 on 16384); ConvRot rows, whose transform makes them issue-bound, keep
-    // more threads per row (64 x 6 / 64 x 8 / 128 x 4 measured slower than this table).
+    // HBM, in 128 x 6 at 98%).  The stand-alone quantize of plain rows takes as many
+    // vectors per thread as fill (the loads a thread has in flight are what keeps HBM
+    // busy: K = 4096 as 64 x 8 instead of 128 x 4 went 0.91 -> 1.00 of HBM on 25900 rows,
+    // K = 2048 as 32 x 8 instead of 64 x 4 0.73 -> 0.87 on 16384).  The layer's
+    // preparation keeps the shallower shapes: each of its blocks also widens a share of
+    // the weight, and with half the blocks the deep shapes gave no faster large-shape
+    // steps and slower small ones (1024x4096x4096 39.8 -> 45.3 us, the preparation no
+    // longer overlapping the GEMM's start).  ConvRot rows, whose transform makes them
+    // issue-bound, keep more threads per row (64 x 6 / 64 x 8 / 128 x 4 measured slower).
     int tpr = 0, vpt = 0;
-    if (rotate) {
+    if (rotate || !OUT8) {
         if (nvec <= 64) { tpr = 32; vpt = 2; }
         else if (nvec <= 128) { tpr = 32; vpt = 4; }
         else if (nvec <= 256) { tpr = 64; vpt = 4; }
@@ -1108,30 +1112,37 @@ cudaError_t rows_dispatch(const void* x, int64_t M, int64_t K, bool rotate, int8
     const unsigned grid = (unsigned)blocks;
 #define CK_ROWS(T, V, R) \
     launch_pdl(rows_kernel<T, V, R, OUT8, OUT16>, grid, THREADS, 0, s, xv, M, K, q8, q16b, xs, w8, w_n16, w16)
+#define CK_SHALLOW(R)                                  \
+    switch (tpr * 16 + vpt) {                          \
+    case 32 * 16 + 2: return CK_ROWS(32, 2, R);        \
+    case 32 * 16 + 4: return CK_ROWS(32, 4, R);        \
+    case 64 * 16 + 4: return CK_ROWS(64, 4, R);        \
+    case 128 * 16 + 3: return CK_ROWS(128, 3, R);      \
+    case 128 * 16 + 4: return CK_ROWS(128, 4, R);      \
+    case 128 * 16 + 6: return CK_ROWS(128, 6, R);      \
+    case 256 * 16 + 4: return CK_ROWS(256, 4, R);      \
+    case 256 * 16 + 6: return CK_ROWS(256, 6, R);      \
+    default: return CK_ROWS(256, 8, R);                \
+    }
     if (rotate) {
+        CK_SHALLOW(true)
+    }
+    if constexpr (!OUT8) {
+        CK_SHALLOW(false)
+    } else {
         switch (tpr * 16 + vpt) {
-        case 32 * 16 + 2: return CK_ROWS(32, 2, true);
-        case 32 * 16 + 4: return CK_ROWS(32, 4, true);
-        case 64 * 16 + 4: return CK_ROWS(64, 4, true);
-        case 128 * 16 + 3: return CK_ROWS(128, 3, true);
-        case 128 * 16 + 4: return CK_ROWS(128, 4, true);
-        case 128 * 16 + 6: return CK_ROWS(128, 6, true);
-        case 256 * 16 + 4: return CK_ROWS(256, 4, true);
-        case 256 * 16 + 6: return CK_ROWS(256, 6, true);
-        default: return CK_ROWS(256, 8, true);
+        case 32 * 16 + 2: return CK_ROWS(32, 2, false);
+        case 32 * 16 + 4: return CK_ROWS(32, 4, false);
+        case 32 * 16 + 8: return CK_ROWS(32, 8, false);
+        case 64 * 16 + 6: return CK_ROWS(64, 6, false);
+        case 64 * 16 + 8: return CK_ROWS(64, 8, false);
+        case 128 * 16 + 6: return CK_ROWS(128, 6, false);
+        case 128 * 16 + 8: return CK_ROWS(128, 8, false);
+        case 256 * 16 + 6: return CK_ROWS(256, 6, false);
+        default: return CK_ROWS(256, 8, false);
         }
     }
-    switch (tpr * 16 + vpt) {
-    case 32 * 16 + 2: return CK_ROWS(32, 2, false);
-    case 32 * 16 + 4: return CK_ROWS(32, 4, false);
-    case 32 * 16 + 8: return CK_ROWS(32, 8, false);
-    case 64 * 16 + 6: return CK_ROWS(64, 6, false);
-    case 64 * 16 + 8: return CK_ROWS(64, 8, false);
-    case 128 * 16 + 6: return CK_ROWS(128, 6, false);
-    case 128 * 16 + 8: return CK_ROWS(128, 8, false);
-    case 256 * 16 + 6: return CK_ROWS(256, 6, false);
-    default: return CK_ROWS(256, 8, false);
-    }
+#undef CK_SHALLOW
 #undef CK_ROWS
 }
 
