@@ -192,7 +192,7 @@ int ck_int8_linear_codes(const void *x, const void *w_codes, const float *w_scal
  *            written.  Page-locked (pinned) host memory lets the copies overlap the
  *            kernels; pageable memory gives the same result with the copies serialized.
  *   w, w_scale, bias, mode, out_dtype: as for ck_int8_linear (device memory); no residual.
- *   slab_rows: rows per pipeline slab (0: about 256 MB of output per slab).  The call
+ *   slab_rows: rows per pipeline slab (0: about 64 MB of output per slab).  The call
  *            cuts M into slabs and overlaps, on two internal copy streams of the current
  *            context (made on its first call there) and the caller's stream, the copy of
  *            slab i+1 to the device, the kernels of slab i and the copy of slab i-1 back.

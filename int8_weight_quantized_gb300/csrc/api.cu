@@ -851,9 +851,11 @@ int64_t host_slab_rows(int64_t M, int64_t N, int out_dtype, int64_t slab_rows)
 {
     if (slab_rows > 0)
         return std::min<int64_t>(slab_rows, std::max<int64_t>(M, 1));
-    // about 256 MB of output per slab, in whole 256-row tile pairs
+    // about 64 MB of output per slab, in whole 256-row tile pairs: against 256 MB the
+    // pipeline fills and drains sooner (median steps on GB300: 80666x28672x5376 25.47 ->
+    // 24.93 ms, 25900x16384x4096 5.34 -> 4.82 ms; the copy back to the host bounds both)
     const int64_t osize = out_dtype == CK_OUT_F32 ? 4 : 2;
-    int64_t r = ((int64_t)256 << 20) / std::max<int64_t>(1, N * osize);
+    int64_t r = ((int64_t)64 << 20) / std::max<int64_t>(1, N * osize);
     r = std::max<int64_t>(256, r / 256 * 256);
     return std::min<int64_t>(r, std::max<int64_t>(M, 1));
 }
