@@ -391,7 +391,9 @@ static bool valid_out_dtype(int t)
 
 // The layer: w8 (int8 codes, widened by the preparation launch) or w_codes (the weight's
 // bf16 codes, prepared once by ck_int8_weight_codes).
-static int linear_impl(const char* name, const void* x, const int8_t* w8, const void* w_codes,
+// The layer, from the int8 weight (own_b16: the preparation launch widens it into the
+// workspace) or from the caller's prepared bf16 weight codes (w_codes).
+static int linear_impl(const char* name, bool own_b16, const void* x, const int8_t* w8, const void* w_codes,
                        const float* w_scale, const void* bias, const void* residual, void* y, int64_t M, int64_t N,
                        int64_t K, int mode, int out_dtype, void* workspace, size_t workspace_bytes, void* stream)
 {
@@ -406,7 +408,6 @@ static int linear_impl(const char* name, const void* x, const int8_t* w8, const 
         return fail(CK_ERR_INVALID_ARG, "ConvRot needs K % 128 == 0 (got %lld)", (long long)K);
     if (M == 0)
         return CK_OK;  // empty batch: x and y may be NULL
-    const bool own_b16 = w_codes == nullptr;
     CK_REQUIRE_PTR(x);
     if (own_b16)
         CK_REQUIRE_PTR(w8);
@@ -481,7 +482,7 @@ int ck_int8_linear(const void* x, const int8_t* w, const float* w_scale, const v
                    void* y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype, void* workspace,
                    size_t workspace_bytes, void* stream)
 {
-    return linear_impl("int8_linear", x, w, nullptr, w_scale, bias, residual, y, M, N, K, mode, out_dtype, workspace,
+    return linear_impl("int8_linear", true, x, w, nullptr, w_scale, bias, residual, y, M, N, K, mode, out_dtype, workspace,
                        workspace_bytes, stream);
 }
 
@@ -519,7 +520,7 @@ int ck_int8_linear_codes(const void* x, const void* w_codes, const float* w_scal
                          const void* residual, void* y, int64_t M, int64_t N, int64_t K, int mode, int out_dtype,
                          void* workspace, size_t workspace_bytes, void* stream)
 {
-    return linear_impl("int8_linear_codes", x, nullptr, w_codes, w_scale, bias, residual, y, M, N, K, mode, out_dtype,
+    return linear_impl("int8_linear_codes", false, x, nullptr, w_codes, w_scale, bias, residual, y, M, N, K, mode, out_dtype,
                        workspace, workspace_bytes, stream);
 }
 

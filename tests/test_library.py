@@ -173,3 +173,26 @@ def test_host_layer_arguments(lib):
     assert st == ck.CK_ERR_INVALID_ARG and "slab_rows" in ck.ck_last_error()
     st = lib.ck_int8_linear_host(ptr, ptr, ptr, None, ptr, 64, 64, 60, ck.PER_ROW, 0, 0, ptr, 1 << 40, None)
     assert st == ck.CK_ERR_INVALID_ARG
+
+
+def test_prepared_weight_entry_points_without_a_gpu(lib):
+    """The layer on prepared weight codes: its workspace holds no widened weight, and bad
+    arguments are rejected before any device work."""
+    import ctypes
+    import int8_weight_quantized_gb300 as ck
+    M, N, K = 1000, 4096, 2048
+    for mode in (ck.TENSORWISE, ck.PER_ROW, ck.CONVROT):
+        full = lib.ck_int8_linear_workspace_size(M, N, K, mode)
+        codes = lib.ck_int8_linear_codes_workspace_size(M, N, K, mode)
+        assert codes > 0 and full - codes >= 2 * N * K  # the bf16 weight codes are the caller's
+    P = ctypes.c_void_p
+    ptr = P(4096)
+    st = lib.ck_int8_linear_codes(ptr, None, ptr, None, None, ptr, 64, 64, 64, ck.PER_ROW, 0, ptr, 1 << 40, None)
+    assert st == ck.CK_ERR_INVALID_ARG and "w_codes" in ck.ck_last_error()
+    st = lib.ck_int8_linear_codes(ptr, P(4100), ptr, None, None, ptr, 64, 64, 64, ck.PER_ROW, 0, ptr, 1 << 40, None)
+    assert st == ck.CK_ERR_INVALID_ARG and "aligned" in ck.ck_last_error()
+    st = lib.ck_int8_linear_codes(ptr, ptr, ptr, None, None, ptr, 64, 64, 64, ck.PER_ROW, 0, ptr, 16, None)
+    assert st == ck.CK_ERR_INVALID_ARG and "workspace" in ck.ck_last_error()
+    st = lib.ck_int8_weight_codes(ptr, 64, 60, ptr, None)
+    assert st == ck.CK_ERR_INVALID_ARG and "16" in ck.ck_last_error()
+    assert lib.ck_int8_weight_codes(ptr, 0, 64, ptr, None) == ck.CK_OK  # no rows: nothing to do
