@@ -49,6 +49,7 @@ FLUSH_BYTES = 512 << 20  # > 129 MB of L2: written between steps (outside the ti
 L2_BYTES = 129 << 20
 CLEAN_BYTES = 256 << 20  # then read, so the step does not start by writing back the flush's dirty lines
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+PROFILE_INT8_PEAK = os.path.join(ROOT, "profiles", "int8_peak.json")
 GEMM_SOURCES = ["int8_weight_quantized_gb300/csrc/gemm.cu", "int8_weight_quantized_gb300/csrc/ck_device.cuh",
                 "int8_weight_quantized_gb300/csrc/gemm_common.cuh"]
 
@@ -97,6 +98,15 @@ def sources_sha256(paths):
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
+
+
+def int8_dense_peak():
+    """GB300's dense int8 matrix rate as measured by the committed mma.sync tool, or None."""
+    try:
+        with open(PROFILE_INT8_PEAK) as f:
+            return json.load(f)["int8_dense_peak"]
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def profiled_traffic(workload):
@@ -395,6 +405,12 @@ def run_ours(args, spec):
                 "peak_sustained": bf16_sust, "frac_sustained": achieved / bf16_sust,
                 "avg_launch_ms": gemm_avg_ms, "timed_launches": g_n,
                 "algorithmic_flops_per_launch": ops}
+    i8 = int8_dense_peak()
+    if i8 is not None and not w8a16:
+        # the GPU's dense int8 matrix rate (its only int8 instruction, mma.sync): the layer,
+        # exact on the bf16 engine, runs at a multiple of it
+        roofline["int8_dense_peak"] = dict(i8, layer_over_peak=value / i8["value"],
+                                           gemm_over_peak=achieved / i8["value"])
     kernels = {
         "gemm": {"ms_per_step": g_ms / kt_steps, "launches": g_n},
         "prep": {"ms_per_step": p_step, "launches": p_n,
