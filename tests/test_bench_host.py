@@ -86,3 +86,19 @@ def test_clock_sample_parser():
 
 def test_profiled_traffic_is_null_for_another_workload():
     assert bench.profiled_traffic("no_such_workload") is None
+
+
+def test_committed_profile_records():
+    """The GEMM traffic record is for the bench default (reported only while it hashes the
+    current GEMM sources); the int8 rate record names its instruction and its summary."""
+    d = json.load(open(bench.PROFILE_TRAFFIC))["gemm"]
+    assert d["workload"] == bench.DEFAULT_WORKLOAD and d["dram_bytes_per_launch"] > 0
+    assert bench.profiled_traffic(bench.DEFAULT_WORKLOAD) in (None, d["dram_bytes_per_launch"])
+    i8 = bench.int8_dense_peak()
+    assert i8 is not None and i8["value"] > 0 and "mma.sync" in i8["instruction"]
+    assert os.path.exists(os.path.join(ROOT, i8["from"]))
+
+
+def test_profiled_traffic_is_null_once_the_gemm_source_changes(monkeypatch):
+    monkeypatch.setattr(bench, "GEMM_SOURCES", bench.GEMM_SOURCES + ["bench.py"])
+    assert bench.profiled_traffic(bench.DEFAULT_WORKLOAD) is None
